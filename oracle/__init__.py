@@ -1,0 +1,138 @@
+"""fp64 CPU oracle for exact attention -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline leg
+may import this package.  The CUDA library never loads, links or calls it, and
+it shares no code with the CUDA path.
+
+Contents
+  * ``forward`` / ``backward``: ctypes front end of ``oracle.c`` -- the plain
+    definition of scaled-dot-product attention and of its gradient, in fp64,
+    parallel over rows / KV heads with OpenMP.
+  * ``naive``: a numpy materialising implementation (S and P as full N x N
+    matrices) used as an independent brute-force check on tiny inputs.
+  * ``online``: the pages' tiled online-softmax recurrences (the FA1 form with
+    separate alpha/beta factors and the FA2 form that divides once at the end),
+    written in numpy fp64, used to check that the recurrence reproduces the
+    definition.
+
+Citations are to the web pages the method is described on:
+  "FlashAttention Primer: IO-Aware Attention, from FA1 to FA4" (oripoin.me),
+  "Flash Attention" (aiwiki.ai), "FlashAttention" concept page (praveentn.live).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False, src: str = _SRC, out: str = _LIB_PATH) -> str:
+    """Compile ``oracle.c`` into ``liboracle.so`` with gcc + OpenMP (fp64, no fast-math)."""
+    if (not force and os.path.exists(out)
+            and os.path.getmtime(out) >= os.path.getmtime(src)):
+        return out
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-fno-fast-math", "-ffp-contract=off", "-fopenmp", "-shared",
+           "-fPIC", "-std=c11", src, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def _as_f64(x) -> np.ndarray:
+    if hasattr(x, "detach"):  # torch tensor: exact widening of the rounded values
+        x = x.detach().to("cpu").double().numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+class Oracle:
+    """ctypes front end of one build of ``oracle.c``."""
+
+    def __init__(self, lib_path: str):
+        lib = ctypes.CDLL(lib_path)
+        dp = ctypes.POINTER(ctypes.c_double)
+        i = ctypes.c_int
+        lib.oracle_forward.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, i, i, ctypes.c_double]
+        lib.oracle_forward.restype = i
+        lib.oracle_backward.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp,
+                                        i, i, i, i, i, i, ctypes.c_double]
+        lib.oracle_backward.restype = i
+        lib.oracle_num_threads.argtypes = []
+        lib.oracle_num_threads.restype = i
+        self.lib = lib
+
+    def num_threads(self) -> int:
+        return int(self.lib.oracle_num_threads())
+
+    def forward(self, q, k, v, causal: bool, scale: float):
+        """O and LSE of softmax(scale q k^T) v, fp64.
+
+        q: [B, Hq, N, d]; k, v: [B, Hkv, N, d].  Returns (o [B,Hq,N,d], lse [B,Hq,N]).
+        LSE is the natural-log log-sum-exp of the scaled scores of each row.
+        """
+        q, k, v = _as_f64(q), _as_f64(k), _as_f64(v)
+        B, Hq, N, d = q.shape
+        Hkv = k.shape[1]
+        assert k.shape == (B, Hkv, N, d) and v.shape == k.shape
+        o = np.empty_like(q)
+        lse = np.empty((B, Hq, N), dtype=np.float64)
+        rc = self.lib.oracle_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                     B, Hq, Hkv, N, d, int(bool(causal)), float(scale))
+        if rc != 0:
+            raise ValueError(f"oracle_forward failed with code {rc}")
+        return o, lse
+
+    def backward(self, q, k, v, dO, causal: bool, scale: float):
+        """dQ, dK, dV (and D = rowsum(dO * O)) of the definition, fp64.
+
+        Recomputes P and O from (q, k, v) itself.  Returns (dq, dk, dv, D).
+        """
+        q, k, v, dO = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(dO)
+        B, Hq, N, d = q.shape
+        Hkv = k.shape[1]
+        assert dO.shape == q.shape and k.shape == (B, Hkv, N, d) and v.shape == k.shape
+        dq = np.empty_like(q)
+        dk = np.empty_like(k)
+        dv = np.empty_like(v)
+        D = np.empty((B, Hq, N), dtype=np.float64)
+        rc = self.lib.oracle_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(dq), _ptr(dk),
+                                      _ptr(dv), _ptr(D), B, Hq, Hkv, N, d,
+                                      int(bool(causal)), float(scale))
+        if rc != 0:
+            raise ValueError(f"oracle_backward failed with code {rc}")
+        return dq, dk, dv, D
+
+
+def _default() -> Oracle:
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = Oracle(build())
+    return _lib
+
+
+def num_threads() -> int:
+    return _default().num_threads()
+
+
+def forward(q, k, v, causal: bool, scale: float):
+    """See ``Oracle.forward``."""
+    return _default().forward(q, k, v, causal, scale)
+
+
+def backward(q, k, v, dO, causal: bool, scale: float):
+    """See ``Oracle.backward``."""
+    return _default().backward(q, k, v, dO, causal, scale)

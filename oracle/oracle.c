@@ -1,0 +1,213 @@
+/*
+ * fp64 CPU oracle for exact scaled-dot-product attention (forward and backward).
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may link, load or call
+ * this file: only the tests, the smoke check and the benchmark's CPU-baseline leg
+ * do.  It shares no code, header, table or helper with the CUDA library.
+ *
+ * What it computes is the plain definition, with no tiling, no online softmax
+ * and no reordering beyond what the definition states:
+ *
+ *   "FlashAttention Primer" (oripoin.me), section "Why attention is quadratic",
+ *   the SDPA equation:      S = Q K^T * scale,  P = rowsoftmax(S),  O = P V
+ *   "Flash Attention" (aiwiki.ai), section "Definition and scope": the same map.
+ *
+ * The saved per-row statistic is the natural-log log-sum-exp of the scaled
+ * scores, LSE_i = m_i + ln(l_i) ("FlashAttention Primer", section "Backward pass:
+ * recomputation instead of storage", which saves O and a per-row log-sum-exp).
+ *
+ * Backward: the gradient of O = softmax(scale Q K^T) V with upstream dO.
+ *   dV_k = sum_i P_ik dO_i
+ *   dP_ik = dO_i . v_k
+ *   D_i  = sum_c dO_ic O_ic  (= sum_k P_ik dP_ik)
+ *   dS_ik = P_ik (dP_ik - D_i)
+ *   dQ_i = scale sum_k dS_ik k_k,   dK_k = scale sum_i dS_ik q_i
+ * The primer's printed backward (Figure 5 and the equation above it) drops the
+ * -D_i term of the softmax Jacobian and the scale factor; this oracle keeps both
+ * (the gradient of the definition), and the tests pin it against finite
+ * differences of the forward, which does not depend on this formula.
+ *
+ * Grouped-query attention: query head h reads KV head floor(h * Hkv / Hq)
+ * (contiguous groups, "Flash Attention" (aiwiki.ai), section "FlashAttention-2",
+ * which covers MQA/GQA where several query heads share one KV head).  dK and dV
+ * of a KV head are the sums over its query heads.
+ *
+ * Causal: key k is visible to query i iff k <= i ("FlashAttention Primer",
+ * section "FlashAttention-1", causal masking paragraph: future scores are -inf).
+ *
+ * Layouts (all row-major, fp64):
+ *   q, o, dO, dq : [B, Hq, N, d]      k, v, dk, dv : [B, Hkv, N, d]
+ *   lse, D       : [B, Hq, N]
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_OK 0
+#define ORACLE_EINVAL 1
+#define ORACLE_ENOMEM 2
+
+static int check_args(int B, int Hq, int Hkv, int N, int d) {
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || N <= 0 || d <= 0) return ORACLE_EINVAL;
+    if (Hq % Hkv != 0) return ORACLE_EINVAL;
+    return ORACLE_OK;
+}
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+static double dot(const double* a, const double* b, int d) {
+    double acc = 0.0;
+    for (int c = 0; c < d; ++c) acc += a[c] * b[c];
+    return acc;
+}
+
+/*
+ * One query row of one head: fills p[0..nk) with the normalised softmax row over
+ * the nk visible keys and returns the row's log-sum-exp.  Plain max-shifted
+ * softmax, evaluated in fp64.
+ */
+static double softmax_row(const double* qi, const double* kh, int nk, int d,
+                          double scale, double* p) {
+    double m = -INFINITY;
+    for (int k = 0; k < nk; ++k) {
+        p[k] = scale * dot(qi, kh + (size_t)k * d, d);
+        if (p[k] > m) m = p[k];
+    }
+    double l = 0.0;
+    for (int k = 0; k < nk; ++k) {
+        p[k] = exp(p[k] - m);
+        l += p[k];
+    }
+    for (int k = 0; k < nk; ++k) p[k] /= l;
+    return m + log(l);
+}
+
+int oracle_forward(const double* q, const double* k, const double* v, double* o,
+                   double* lse, int B, int Hq, int Hkv, int N, int d, int causal,
+                   double scale) {
+    int rc = check_args(B, Hq, Hkv, N, d);
+    if (rc) return rc;
+    if (!q || !k || !v || !o || !lse) return ORACLE_EINVAL;
+    const int64_t rows = (int64_t)B * Hq * N;
+    int failed = 0;
+#pragma omp parallel
+    {
+        double* p = (double*)malloc(sizeof(double) * (size_t)N);
+        if (!p) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(dynamic, 16)
+        for (int64_t r = 0; r < rows; ++r) {
+            if (!p) continue;
+            const int i = (int)(r % N);
+            const int64_t bh = r / N;
+            const int h = (int)(bh % Hq);
+            const int b = (int)(bh / Hq);
+            const int g = (int)(((int64_t)h * Hkv) / Hq);
+            const double* qi = q + (size_t)r * d;
+            const double* kh = k + ((size_t)b * Hkv + g) * (size_t)N * d;
+            const double* vh = v + ((size_t)b * Hkv + g) * (size_t)N * d;
+            const int nk = causal ? i + 1 : N;
+            lse[r] = softmax_row(qi, kh, nk, d, scale, p);
+            double* oi = o + (size_t)r * d;
+            for (int c = 0; c < d; ++c) oi[c] = 0.0;
+            for (int kk = 0; kk < nk; ++kk) {
+                const double w = p[kk];
+                const double* vk = vh + (size_t)kk * d;
+                for (int c = 0; c < d; ++c) oi[c] += w * vk[c];
+            }
+        }
+        free(p);
+    }
+    return failed ? ORACLE_ENOMEM : ORACLE_OK;
+}
+
+/*
+ * Backward from the definition.  Recomputes P and O itself from (q, k, v); it
+ * takes no forward output from anywhere else.  D (may be NULL) receives
+ * D_i = dO_i . O_i.  Parallel over (b, kv-head) so that dK/dV of a KV head are
+ * accumulated by one thread, summing its query-head group in order.
+ */
+int oracle_backward(const double* q, const double* k, const double* v, const double* dO,
+                    double* dq, double* dk, double* dv, double* D, int B, int Hq,
+                    int Hkv, int N, int d, int causal, double scale) {
+    int rc = check_args(B, Hq, Hkv, N, d);
+    if (rc) return rc;
+    if (!q || !k || !v || !dO || !dq || !dk || !dv) return ORACLE_EINVAL;
+    const int group = Hq / Hkv;
+    const int64_t heads = (int64_t)B * Hkv;
+    int failed = 0;
+#pragma omp parallel
+    {
+        double* p = (double*)malloc(sizeof(double) * (size_t)N);
+        double* ds = (double*)malloc(sizeof(double) * (size_t)N);
+        double* oi = (double*)malloc(sizeof(double) * (size_t)d);
+        if (!p || !ds || !oi) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t bg = 0; bg < heads; ++bg) {
+            if (!p || !ds || !oi) continue;
+            const int64_t b = bg / Hkv;
+            const int g = (int)(bg % Hkv);
+            const double* kh = k + (size_t)bg * N * d;
+            const double* vh = v + (size_t)bg * N * d;
+            double* dkh = dk + (size_t)bg * N * d;
+            double* dvh = dv + (size_t)bg * N * d;
+            memset(dkh, 0, sizeof(double) * (size_t)N * d);
+            memset(dvh, 0, sizeof(double) * (size_t)N * d);
+            for (int hh = 0; hh < group; ++hh) {
+                const int h = g * group + hh;
+                const size_t head = ((size_t)b * Hq + h) * (size_t)N;
+                for (int i = 0; i < N; ++i) {
+                    const double* qi = q + (head + i) * d;
+                    const double* doi = dO + (head + i) * d;
+                    double* dqi = dq + (head + i) * d;
+                    const int nk = causal ? i + 1 : N;
+                    softmax_row(qi, kh, nk, d, scale, p);
+                    /* O_i = sum_k P_ik v_k, then D_i = dO_i . O_i */
+                    for (int c = 0; c < d; ++c) oi[c] = 0.0;
+                    for (int kk = 0; kk < nk; ++kk)
+                        for (int c = 0; c < d; ++c) oi[c] += p[kk] * vh[(size_t)kk * d + c];
+                    const double Di = dot(doi, oi, d);
+                    if (D) D[head + i] = Di;
+                    /* dS_ik = P_ik (dO_i . v_k - D_i) */
+                    for (int kk = 0; kk < nk; ++kk)
+                        ds[kk] = p[kk] * (dot(doi, vh + (size_t)kk * d, d) - Di);
+                    /* dQ_i = scale sum_k dS_ik k_k */
+                    for (int c = 0; c < d; ++c) dqi[c] = 0.0;
+                    for (int kk = 0; kk < nk; ++kk)
+                        for (int c = 0; c < d; ++c) dqi[c] += ds[kk] * kh[(size_t)kk * d + c];
+                    for (int c = 0; c < d; ++c) dqi[c] *= scale;
+                    /* dK_k += scale dS_ik q_i ; dV_k += P_ik dO_i */
+                    for (int kk = 0; kk < nk; ++kk) {
+                        const double a = scale * ds[kk];
+                        const double w = p[kk];
+                        double* dkk = dkh + (size_t)kk * d;
+                        double* dvk = dvh + (size_t)kk * d;
+                        for (int c = 0; c < d; ++c) {
+                            dkk[c] += a * qi[c];
+                            dvk[c] += w * doi[c];
+                        }
+                    }
+                }
+            }
+        }
+        free(p);
+        free(ds);
+        free(oi);
+    }
+    return failed ? ORACLE_ENOMEM : ORACLE_OK;
+}

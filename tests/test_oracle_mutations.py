@@ -1,0 +1,87 @@
+"""Plant plausible mistakes in copies of the oracle and check the pins catch each one.
+
+Every mutation is applied to the C source text, compiled into a throw-away
+library on the CPU, and run through three independent checks: the materialising
+numpy schedule, finite differences of the forward, and the closed form for
+identical keys.  A mutation that none of them flags would mean the pins have a
+blind spot.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import naive
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
+
+# (name, exact text in oracle.c, replacement)
+MUTATIONS = [
+    ("drop_D_term", "- Di);", ");"),
+    ("drop_dq_scale", "dqi[c] *= scale;", "dqi[c] *= 1.0;"),
+    ("dk_without_scale", "const double a = scale * ds[kk];", "const double a = ds[kk];"),
+    ("dv_uses_q", "dvk[c] += w * doi[c];", "dvk[c] += w * qi[c];"),
+    ("causal_off_by_one", "const int nk = causal ? i + 1 : N;\n            lse",
+     "const int nk = causal ? i : N;\n            lse"),
+    ("lse_without_max", "return m + log(l);", "return log(l);"),
+    ("no_max_shift", "p[k] = exp(p[k] - m);", "p[k] = exp(p[k]);"),
+    ("gqa_modulo_map", "const int g = (int)(((int64_t)h * Hkv) / Hq);",
+     "const int g = (int)(h % Hkv);"),
+    ("unnormalised_p", "for (int k = 0; k < nk; ++k) p[k] /= l;", ""),
+    ("transposed_dq_operand", "dqi[c] += ds[kk] * kh[(size_t)kk * d + c];",
+     "dqi[c] += ds[kk] * vh[(size_t)kk * d + c];"),
+]
+
+
+def _checks_fail(o: "oracle.Oracle") -> bool:
+    rng = np.random.default_rng(99)
+    B, Hq, Hkv, N, d, s = 1, 4, 2, 6, 3, 0.8
+    q, k, v, dO = (rng.standard_normal(x) for x in
+                   ((B, Hq, N, d), (B, Hkv, N, d), (B, Hkv, N, d), (B, Hq, N, d)))
+    # Large-magnitude queries make a missing max-shift overflow.
+    q_big = 300.0 * q
+    for causal in (False, True):
+        for qq in (q, q_big):
+            try:
+                got_o, got_lse = o.forward(qq, k, v, causal, s)
+            except ValueError:
+                return True
+            ref_o, ref_lse, _ = naive.forward(qq, k, v, causal, s)
+            if not (np.allclose(got_o, ref_o, atol=1e-9) and np.allclose(got_lse, ref_lse, atol=1e-9)):
+                return True
+        dq, dk, dv, _ = o.backward(q, k, v, dO, causal, s)
+        h = 1e-6
+        for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+            idx = tuple(int(rng.integers(0, n)) for n in x.shape)
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            args = dict(q=q, k=k, v=v)
+            args[name] = xp
+            lp = float((oracle.forward(args["q"], args["k"], args["v"], causal, s)[0] * dO).sum())
+            args[name] = xm
+            lm = float((oracle.forward(args["q"], args["k"], args["v"], causal, s)[0] * dO).sum())
+            if abs((lp - lm) / (2 * h) - g[idx]) > 1e-5 * max(1.0, abs(g[idx])):
+                return True
+        ref = naive.backward(q, k, v, dO, causal, s)
+        for a, b in zip((dq, dk, dv), ref[:3]):
+            if not np.allclose(a, b, atol=1e-9):
+                return True
+    return False
+
+
+@pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_planted_mistake_is_caught(tmp_path, name, old, new):
+    text = open(SRC).read()
+    assert text.count(old) == 1, f"mutation anchor for {name} not unique in oracle.c"
+    src = tmp_path / f"oracle_{name}.c"
+    src.write_text(text.replace(old, new))
+    lib = oracle.build(force=True, src=str(src), out=str(tmp_path / f"lib_{name}.so"))
+    assert _checks_fail(oracle.Oracle(lib)), f"pins did not catch mutation {name}"
+
+
+def test_unmutated_oracle_passes_the_same_checks(tmp_path):
+    lib = oracle.build(force=True, src=SRC, out=str(tmp_path / "lib_clean.so"))
+    assert not _checks_fail(oracle.Oracle(lib))
