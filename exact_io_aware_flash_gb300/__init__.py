@@ -1,2 +1,12 @@
-"""Exact IO-aware attention for GB300 (sm_103a): forward with online softmax + LSE,
-recomputing backward, behind the C ABI of ``libfa.so``."""
+"""Exact IO-aware attention for GB300 (sm_103a).
+
+Forward with online softmax and per-row log-sum-exp, recomputing backward, both
+in hand-written tcgen05/TMEM/TMA kernels behind the C ABI of ``libfa.so``
+(``include/fa.h``).  Python here only marshals arguments.
+
+    from exact_io_aware_flash_gb300 import forward, backward
+    o, lse = forward(q, k, v, causal=True)
+    dq, dk, dv = backward(q, k, v, o, lse, dO, causal=True)
+"""
+from ._lib import (FAError, backward, check_errors, forward, load, version,  # noqa: F401
+                   workspace_size)

@@ -1,0 +1,160 @@
+"""ctypes binding of libfa.so: argument marshalling only.
+
+Every step of the attention path runs in the library's CUDA kernels; this
+module checks tensors, allocates outputs with torch, and passes raw device
+pointers and the current CUDA stream through the C ABI declared in
+``include/fa.h``.  If the library is missing it raises: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libfa.so")
+
+FA_OK, FA_ERR_INVALID, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = 0, 1, 2, 3, 4
+FA_DTYPE_FP16, FA_DTYPE_BF16 = 0, 1
+_CODES = {FA_ERR_INVALID: "FA_ERR_INVALID", FA_ERR_UNSUPPORTED: "FA_ERR_UNSUPPORTED",
+          FA_ERR_CUDA: "FA_ERR_CUDA", FA_ERR_TIMEOUT: "FA_ERR_TIMEOUT"}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class FAError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{_CODES.get(code, code)}: {msg}")
+        self.code = code
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libfa.so (built by ``exact_io_aware_flash_gb300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"{path} not found: the CUDA library is required (build it with "
+                "`python -m exact_io_aware_flash_gb300.build`); there is no CPU fallback")
+        lib = ctypes.CDLL(path)
+        vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        lib.fa_forward.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp]
+        lib.fa_forward.restype = i
+        lib.fa_backward_workspace_size.argtypes = [i, i, i, i]
+        lib.fa_backward_workspace_size.restype = sz
+        lib.fa_backward.argtypes = [vp] * 10 + [sz] + [i] * 7 + [f, i, vp]
+        lib.fa_backward.restype = i
+        lib.fa_check_errors.argtypes = [vp]
+        lib.fa_check_errors.restype = i
+        lib.fa_last_error.argtypes = []
+        lib.fa_last_error.restype = ctypes.c_char_p
+        lib.fa_version.argtypes = []
+        lib.fa_version.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def _raise(code: int):
+    if code != FA_OK:
+        raise FAError(code, load().fa_last_error().decode())
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float16:
+        return FA_DTYPE_FP16
+    if t.dtype == torch.bfloat16:
+        return FA_DTYPE_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}: use float16 or bfloat16")
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _check(t: torch.Tensor, name: str, shape, dtype):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous [B, H, N, d]")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+
+
+def version() -> str:
+    return load().fa_version().decode()
+
+
+def workspace_size(B: int, Hq: int, N: int, d: int) -> int:
+    return int(load().fa_backward_workspace_size(B, Hq, N, d))
+
+
+def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
+            stream=None):
+    """O = softmax(scale q k^T) v and the natural-log LSE per row, on the GPU.
+
+    q: [B, Hq, N, d]; k, v: [B, Hkv, N, d]; fp16 or bf16, contiguous, CUDA.
+    Returns (o [B,Hq,N,d] in q's dtype, lse [B,Hq,N] float32).
+    """
+    B, Hq, N, d = q.shape
+    Hkv = k.shape[1]
+    _check(q, "q", (B, Hq, N, d), q.dtype)
+    _check(k, "k", (B, Hkv, N, d), q.dtype)
+    _check(v, "v", (B, Hkv, N, d), q.dtype)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device)
+    _check(out, "out", (B, Hq, N, d), q.dtype)
+    _check(lse, "lse", (B, Hq, N), torch.float32)
+    rc = load().fa_forward(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                           lse.data_ptr(), B, Hq, Hkv, N, d, int(bool(causal)), float(scale),
+                           _dtype_code(q), _stream_handle(stream))
+    _raise(rc)
+    return out, lse
+
+
+def backward(q, k, v, o, lse, dO, causal: bool = False, scale: float | None = None, dq=None,
+             dk=None, dv=None, workspace=None, stream=None):
+    """dq, dk, dv of O = softmax(scale q k^T) v given the forward's o, lse and dO = dL/dO."""
+    B, Hq, N, d = q.shape
+    Hkv = k.shape[1]
+    for t, name, H in ((q, "q", Hq), (k, "k", Hkv), (v, "v", Hkv), (o, "o", Hq), (dO, "dO", Hq)):
+        _check(t, name, (B, H, N, d), q.dtype)
+    _check(lse, "lse", (B, Hq, N), torch.float32)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _check(dq, "dq", (B, Hq, N, d), q.dtype)
+    _check(dk, "dk", (B, Hkv, N, d), q.dtype)
+    _check(dv, "dv", (B, Hkv, N, d), q.dtype)
+    ws_bytes = workspace_size(B, Hq, N, d)
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    if workspace.numel() * workspace.element_size() < ws_bytes:
+        raise ValueError(f"workspace must hold at least {ws_bytes} bytes")
+    rc = load().fa_backward(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                            dO.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                            workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                            B, Hq, Hkv, N, d, int(bool(causal)), float(scale), _dtype_code(q),
+                            _stream_handle(stream))
+    _raise(rc)
+    return dq, dk, dv
+
+
+def check_errors(stream=None) -> None:
+    """Synchronise the stream and raise FAError if a kernel's bounded wait expired."""
+    _raise(load().fa_check_errors(_stream_handle(stream)))

@@ -1,0 +1,228 @@
+// C ABI of libfa.so (declared in include/fa.h): argument checks, Tensor Memory
+// Accelerator descriptor encoding, the device error word, and kernel launches.
+// Host code only; the kernels live in fa_fwd.cu and fa_bwd.cu.
+#include "../../include/fa.h"
+#include "fa_internal.h"
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+namespace {
+
+// Device error word: set by a kernel whose bounded wait expired.  One per
+// device (a __device__ variable is instantiated in every context).
+__device__ int g_fa_error_word;
+
+thread_local std::string t_last_error;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+  return code;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  std::once_flag once;
+  int status = FA_OK;
+  std::string msg;
+  int* err_word = nullptr;
+};
+
+DeviceState g_dev[kMaxDevices];
+EncodeTiledFn g_encode = nullptr;
+std::once_flag g_encode_once;
+std::string g_encode_msg;
+
+int get_device_state(DeviceState** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(FA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return fail(FA_ERR_UNSUPPORTED, "device index %d", dev);
+  DeviceState& st = g_dev[dev];
+  std::call_once(st.once, [&st, dev]() {
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (major != 10 || minor != 3) {
+      st.status = FA_ERR_UNSUPPORTED;
+      st.msg = "device " + std::to_string(dev) + " is sm_" + std::to_string(major) +
+               std::to_string(minor) + "; this library is built for sm_103a only";
+      return;
+    }
+    void* p = nullptr;
+    cudaError_t ee = cudaGetSymbolAddress(&p, g_fa_error_word);
+    if (ee != cudaSuccess) {
+      st.status = FA_ERR_CUDA;
+      st.msg = std::string("cudaGetSymbolAddress(error word): ") + cudaGetErrorString(ee);
+      return;
+    }
+    st.err_word = static_cast<int*>(p);
+  });
+  if (st.status != FA_OK) return fail(st.status, "%s", st.msg.c_str());
+  std::call_once(g_encode_once, []() {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t ee =
+        cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (ee != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr) {
+      g_encode_msg = "cuTensorMapEncodeTiled entry point not available";
+      return;
+    }
+    g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  });
+  if (!g_encode) return fail(FA_ERR_CUDA, "%s", g_encode_msg.c_str());
+  *out = &st;
+  return FA_OK;
+}
+
+// [heads, N, d] 16-bit tensor, box {64, 128, 1}, 128-byte swizzle, zero fill out of bounds.
+int encode_tile_map(CUtensorMap* map, const void* base, int heads, int N, int d, int bf16,
+                    const char* name) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                        static_cast<cuuint64_t>(heads)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                           static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                        3, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed: %d", name, (int)r);
+  return FA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_common(int B, int Hq, int Hkv, int N, int d, float scale, int dtype) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || N <= 0)
+    return fail(FA_ERR_INVALID, "sizes must be positive (B=%d Hq=%d Hkv=%d N=%d)", B, Hq, Hkv, N);
+  if (Hq % Hkv != 0) return fail(FA_ERR_INVALID, "Hq (%d) must be a multiple of Hkv (%d)", Hq, Hkv);
+  if (!std::isfinite(scale)) return fail(FA_ERR_INVALID, "scale must be finite");
+  if (d != 64 && d != 128) return fail(FA_ERR_UNSUPPORTED, "head dimension d=%d (supported: 64, 128)", d);
+  if (dtype != FA_DTYPE_FP16 && dtype != FA_DTYPE_BF16)
+    return fail(FA_ERR_UNSUPPORTED, "dtype %d (supported: FA_DTYPE_FP16, FA_DTYPE_BF16)", dtype);
+  // grid.y carries pairs of 128-row query tiles; grid.x carries B*Hq.
+  const long long pairs = ((long long)N + 255) / 256;
+  if (pairs > 65535) return fail(FA_ERR_UNSUPPORTED, "N=%d exceeds the supported maximum", N);
+  if ((long long)B * Hq > 0x7fffffffLL || (long long)B * Hq * N > 0x7fffffffLL)
+    return fail(FA_ERR_UNSUPPORTED, "B*Hq*N exceeds 2^31-1");
+  return FA_OK;
+}
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
+
+extern "C" {
+
+const char* fa_version(void) { return "fa-gb300 0.1.0 (sm_103a, tcgen05/TMEM/TMA)"; }
+
+const char* fa_last_error(void) { return t_last_error.c_str(); }
+
+int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+               int Hkv, int N, int d, int causal, float scale, int dtype, void* stream) {
+  t_last_error.clear();
+  if (!q || !k || !v || !o || !lse) return fail(FA_ERR_INVALID, "null tensor pointer");
+  int rc = check_common(B, Hq, Hkv, N, d, scale, dtype);
+  if (rc) return rc;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return fail(FA_ERR_UNSUPPORTED, "all tensor pointers must be 16-byte aligned");
+  DeviceState* st = nullptr;
+  if ((rc = get_device_state(&st))) return rc;
+  fa::AttnShape s{B, Hq, Hkv, N, d, causal ? 1 : 0, scale, dtype == FA_DTYPE_BF16};
+  fa::FwdArgs a{};
+  if ((rc = encode_tile_map(&a.tm_q, q, B * Hq, N, d, s.bf16, "q"))) return rc;
+  if ((rc = encode_tile_map(&a.tm_k, k, B * Hkv, N, d, s.bf16, "k"))) return rc;
+  if ((rc = encode_tile_map(&a.tm_v, v, B * Hkv, N, d, s.bf16, "v"))) return rc;
+  a.o = o;
+  a.lse = lse;
+  a.err = st->err_word;
+  cudaError_t e = fa::launch_forward(s, a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(FA_ERR_CUDA, "forward launch: %s", cudaGetErrorString(e));
+  return FA_OK;
+}
+
+size_t fa_backward_workspace_size(int B, int Hq, int N, int d) {
+  if (B <= 0 || Hq <= 0 || N <= 0 || d <= 0) return 0;
+  const size_t rows = static_cast<size_t>(B) * Hq * N;
+  return round_up(rows * 4, 256) + rows * static_cast<size_t>(d) * 4;
+}
+
+int fa_backward(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                const void* dO, void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
+                int B, int Hq, int Hkv, int N, int d, int causal, float scale, int dtype,
+                void* stream) {
+  t_last_error.clear();
+  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv || !workspace)
+    return fail(FA_ERR_INVALID, "null tensor pointer");
+  int rc = check_common(B, Hq, Hkv, N, d, scale, dtype);
+  if (rc) return rc;
+  const size_t need = fa_backward_workspace_size(B, Hq, N, d);
+  if (ws_bytes < need)
+    return fail(FA_ERR_INVALID, "workspace of %zu bytes is smaller than the %zu required", ws_bytes, need);
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(FA_ERR_UNSUPPORTED, "workspace must be 256-byte aligned");
+  const void* ptrs[] = {q, k, v, o, lse, dO, dq, dk, dv};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return fail(FA_ERR_UNSUPPORTED, "all tensor pointers must be 16-byte aligned");
+  DeviceState* st = nullptr;
+  if ((rc = get_device_state(&st))) return rc;
+  fa::AttnShape s{B, Hq, Hkv, N, d, causal ? 1 : 0, scale, dtype == FA_DTYPE_BF16};
+  fa::BwdArgs a{};
+  if ((rc = encode_tile_map(&a.tm_q, q, B * Hq, N, d, s.bf16, "q"))) return rc;
+  if ((rc = encode_tile_map(&a.tm_k, k, B * Hkv, N, d, s.bf16, "k"))) return rc;
+  if ((rc = encode_tile_map(&a.tm_v, v, B * Hkv, N, d, s.bf16, "v"))) return rc;
+  if ((rc = encode_tile_map(&a.tm_do, dO, B * Hq, N, d, s.bf16, "dO"))) return rc;
+  const size_t rows = static_cast<size_t>(B) * Hq * N;
+  a.o = o;
+  a.dO = dO;
+  a.lse = lse;
+  a.D = static_cast<float*>(workspace);
+  a.dq_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + round_up(rows * 4, 256));
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.err = st->err_word;
+  cudaError_t e = fa::launch_backward(s, a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(FA_ERR_CUDA, "backward launch: %s", cudaGetErrorString(e));
+  return FA_OK;
+}
+
+int fa_check_errors(void* stream) {
+  t_last_error.clear();
+  DeviceState* st = nullptr;
+  int rc = get_device_state(&st);
+  if (rc) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return fail(FA_ERR_CUDA, "stream synchronize: %s", cudaGetErrorString(e));
+  int word = 0;
+  e = cudaMemcpyFromSymbolAsync(&word, g_fa_error_word, sizeof(int), 0, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return fail(FA_ERR_CUDA, "reading the error word: %s", cudaGetErrorString(e));
+  if (word != 0) {
+    const int zero = 0;
+    cudaMemcpyToSymbolAsync(g_fa_error_word, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, s);
+    cudaStreamSynchronize(s);
+    return fail(FA_ERR_TIMEOUT, "a kernel's bounded wait expired (device error word %d)", word);
+  }
+  return FA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,402 @@
+// Forward kernel: exact attention with online softmax on tcgen05 tensor cores.
+//
+// What it computes ("FlashAttention Primer: IO-Aware Attention, from FA1 to FA4",
+// sections "Why attention is quadratic" and "FlashAttention-1"; "Flash Attention"
+// (aiwiki.ai), section "Online softmax"): for every query row i,
+//     O_i = sum_k softmax_k(scale * q_i . k_k) v_k,   LSE_i = ln sum_k exp(scale * q_i . k_k)
+// by streaming key/value tiles through shared memory and carrying a running row
+// maximum m, running sum l and an unnormalised accumulator O (the FA2 form: P is
+// exponentiated against the running maximum and O is divided by l once at the
+// end, "Flash Attention", section "Online softmax").
+//
+// GB300 design (one CTA per pair of 128-row query tiles of one head):
+//   warp 8      TMA producer: Q tiles once, then K_j and V_j through two
+//               2-stage shared-memory rings (128-byte swizzle, 3-D tensor maps
+//               over [B*H, N, d] so ragged tails are zero-filled).
+//   warp 9      MMA issuer (one thread): S_X = Q_X K_j^T into Tensor Memory,
+//               O_X += P_X V_j with P_X read from Tensor Memory (A operand) and
+//               V_j from shared memory as an MN-major B operand.
+//   warps 0-3   softmax for query tile A, warps 4-7 for tile B: thread t owns
+//               row t (TMEM lane t); exp2 with the scale folded in; P written
+//               back to TMEM as 16-bit pairs over the first half of S.
+// The two tiles ping-pong: while one softmax group works, the tensor core runs
+// the other tile's MMAs ("FlashAttention Primer", section "FlashAttention-3":
+// softmax of one block overlaps the matmuls of another; Figure 7).
+//
+// Conditional rescaling ("Flash Attention", section "FlashAttention-4": skip the
+// O rescale unless the running maximum grows by more than log2(256) = 8 in the
+// exp2 domain): exact, since O and l always share the same reference maximum.
+//
+// Causal ("FlashAttention Primer", section "FlashAttention-1", causal
+// paragraph): key tiles above the diagonal are never loaded or computed; only
+// the diagonal tile and the ragged last tile are masked element-wise.
+#include "fa_internal.h"
+#include "ptx.cuh"
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+namespace fa {
+namespace {
+
+constexpr int kBM = 128;           // query rows per tile
+constexpr int kBN = 128;           // keys per tile
+constexpr int kAtomBytes = 16384;  // 128 rows x 128 bytes: 64 columns of one 16-bit tile
+constexpr int kThreads = 320;      // 10 warps
+constexpr int kStages = 2;
+
+template <int D>
+struct FwdSmem {
+  static constexpr int kTile = kBM * D * 2;  // bytes of one 128 x D 16-bit tile
+  static constexpr int kQ = 0;               // 2 query tiles
+  static constexpr int kK = kQ + 2 * kTile;  // K ring
+  static constexpr int kV = kK + kStages * kTile;
+  static constexpr int kBar = kV + kStages * kTile;
+  static constexpr int kBytes = kBar + 256;
+  static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
+};
+
+enum Bars {
+  BQ = 0,
+  BKFULL = 1,   // +stage
+  BKEMPTY = 3,  // +stage
+  BVFULL = 5,
+  BVEMPTY = 7,
+  BSFULL = 9,   // +tile
+  BPFULL = 11,  // +tile
+  BODONE = 13,  // +tile
+  BFINAL = 15,
+  NBARS = 16
+};
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (BF16) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  } else {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+}
+
+// Bounded wait used only while tearing down after an abort: ignores the abort
+// flag so that copies already in flight land before the CTA exits.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const unsigned long long t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > 200000000ull) break;
+  }
+}
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, void* __restrict__ out,
+                  float* __restrict__ lse_out, int Hq, int Hkv, int N, int causal,
+                  float scale_log2, int* err) {
+  using L = FwdSmem<D>;
+  constexpr int kAtoms = D / 64;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::kBar);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + NBARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int bh = blockIdx.x;  // b * Hq + h
+  const int pair = gridDim.y - 1 - blockIdx.y;  // heaviest causal pairs first
+  const int h = bh % Hq;
+  const int b = bh / Hq;
+  const int kvh = b * Hkv + h / (Hq / Hkv);
+  const int T = (N + kBM - 1) / kBM;
+  const int tA = 2 * pair, tB = 2 * pair + 1;
+  const bool hasB = tB < T;
+  const int nA = causal ? tA + 1 : T;
+  const int nB = hasB ? (causal ? tB + 1 : T) : 0;
+  const int nKV = nA > nB ? nA : nB;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NBARS; ++i) mbar_init(&bar[i], (i == BPFULL || i == BPFULL + 1) ? 4 : 1);
+    *abort_flag = (*reinterpret_cast<volatile int*>(err) != kDevErrNone) ? 1 : 0;
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const bool run = (*abort_flag == 0);
+
+  if (run && warp == 8) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      const uint64_t pol_q = l2_policy_evict_first();
+      const uint64_t pol_kv = l2_policy_evict_last();
+      mbar_expect_tx(&bar[BQ], L::kTile * (hasB ? 2 : 1));
+      for (int a = 0; a < kAtoms; ++a) {
+        tma_load_3d(smem + L::kQ + a * kAtomBytes, &tm_q, &bar[BQ], a * 64, tA * kBM, bh, pol_q);
+        if (hasB)
+          tma_load_3d(smem + L::kQ + L::kTile + a * kAtomBytes, &tm_q, &bar[BQ], a * 64, tB * kBM,
+                      bh, pol_q);
+      }
+      int issued = 0;
+      for (int j = 0; j < nKV; ++j) {
+        const int st = j & 1;
+        const uint32_t ph = (j >> 1) & 1;
+        if (!mbar_wait(&bar[BKEMPTY + st], ph ^ 1, abort_flag, err)) break;
+        mbar_expect_tx(&bar[BKFULL + st], L::kTile);
+        for (int a = 0; a < kAtoms; ++a)
+          tma_load_3d(smem + L::kK + st * L::kTile + a * kAtomBytes, &tm_k, &bar[BKFULL + st],
+                      a * 64, j * kBN, kvh, pol_kv);
+        if (!mbar_wait(&bar[BVEMPTY + st], ph ^ 1, abort_flag, err)) {
+          issued = 2 * j + 1;
+          break;
+        }
+        mbar_expect_tx(&bar[BVFULL + st], L::kTile);
+        for (int a = 0; a < kAtoms; ++a)
+          tma_load_3d(smem + L::kV + st * L::kTile + a * kAtomBytes, &tm_v, &bar[BVFULL + st],
+                      a * 64, j * kBN, kvh, pol_kv);
+        issued = 2 * j + 2;
+      }
+      if (*abort_flag) {
+        // Let every copy already issued land before shared memory is released.
+        drain_wait(&bar[BQ], 0);
+        for (int i = (issued > 4 ? issued - 4 : 0); i < issued; ++i) {
+          const int j = i >> 1, st = j & 1;
+          drain_wait(&bar[((i & 1) ? BVFULL : BKFULL) + st], (j >> 1) & 1);
+        }
+      }
+    }
+  } else if (run && warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdS = idesc_f16(kBM, kBN, BF16, false, false);
+      constexpr uint32_t kIdO = idesc_f16(kBM, D, BF16, false, true);
+      const uint32_t sq = smem_u32(smem + L::kQ);
+      const uint32_t sk = smem_u32(smem + L::kK);
+      const uint32_t sv = smem_u32(smem + L::kV);
+
+      auto issue_s = [&](int X, int st) {
+        const uint32_t dt = tmem + X * 128;
+        const uint32_t qa = sq + X * L::kTile;
+        const uint32_t ka = sk + st * L::kTile;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * kAtomBytes + (ks & 3) * 32;
+          mma_ss(dt, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), kIdS,
+                 ks > 0);
+        }
+        mma_commit(&bar[BSFULL + X]);
+      };
+      auto issue_pv = [&](int X, int st, int j) {
+        const uint32_t dt = tmem + 256 + X * 128;
+        const uint32_t pt = tmem + X * 128;
+        const uint32_t va = sv + st * L::kTile;
+#pragma unroll
+        for (int ks = 0; ks < kBN / 16; ++ks)
+          mma_ts(dt, pt + ks * 8, sdesc_sw128(va + ks * 2048, kAtomBytes, 1024), kIdO,
+                 (j > 0 || ks > 0) ? 1u : 0u);
+        mma_commit(&bar[BODONE + X]);
+      };
+
+      bool ok = mbar_wait(&bar[BQ], 0, abort_flag, err) &&
+                mbar_wait(&bar[BKFULL], 0, abort_flag, err);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0, 0);
+        if (nB > 0) issue_s(1, 0);
+        mma_commit(&bar[BKEMPTY]);
+      }
+      for (int j = 0; ok && j < nKV; ++j) {
+        const int st = j & 1;
+        const uint32_t ph = (j >> 1) & 1;
+        if (!(ok = mbar_wait(&bar[BVFULL + st], ph, abort_flag, err))) break;
+        if (j < nA) {
+          if (!(ok = mbar_wait(&bar[BPFULL], j & 1, abort_flag, err))) break;
+          tc_fence_after();
+          issue_pv(0, st, j);
+        }
+        if (j < nB) {
+          if (!(ok = mbar_wait(&bar[BPFULL + 1], j & 1, abort_flag, err))) break;
+          tc_fence_after();
+          issue_pv(1, st, j);
+        }
+        mma_commit(&bar[BVEMPTY + st]);
+        if (j + 1 < nKV) {
+          const int st1 = (j + 1) & 1;
+          const uint32_t ph1 = ((j + 1) >> 1) & 1;
+          if (!(ok = mbar_wait(&bar[BKFULL + st1], ph1, abort_flag, err))) break;
+          // S_X(j+1) overwrites the columns P_X(j) was read from: wait for PV_X(j).
+          if (j + 1 < nA) {
+            if (!(ok = mbar_wait(&bar[BODONE], j & 1, abort_flag, err))) break;
+            tc_fence_after();
+            issue_s(0, st1);
+          }
+          if (j + 1 < nB) {
+            if (!(ok = mbar_wait(&bar[BODONE + 1], j & 1, abort_flag, err))) break;
+            tc_fence_after();
+            issue_s(1, st1);
+          }
+          mma_commit(&bar[BKEMPTY + st1]);
+        }
+      }
+      // Every MMA this thread issued has completed before TMEM is released.
+      mma_commit(&bar[BFINAL]);
+      drain_wait(&bar[BFINAL], 0);
+    }
+  } else if (run && warp < 8) {
+    // ------------------------------------------------------------ softmax
+    const int X = warp >> 2;
+    const int t = X ? tB : tA;
+    const int nX = X ? nB : nA;
+    const int r = threadIdx.x & 127;
+    const int q = t * kBM + r;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_off + X * 128;
+    const uint32_t tO = tmem + lane_off + 256 + X * 128;
+    float m_run = -INFINITY;
+    float l_run = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nX; ++j) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&bar[BSFULL + X], j & 1, abort_flag, err));
+      if (!ok) break;
+      tc_fence_after();
+      // x holds the scores as raw bits: s * scale * log2(e) after the first pass.
+      uint32_t x[kBN];
+#pragma unroll
+      for (int c = 0; c < kBN; c += 32) tmem_ld32(tS + c, x + c);
+      tmem_ld_wait();
+      reg_fence<kBN>(x);
+      const int kbase = j * kBN;
+      const bool diag = causal && (j == t);
+      int lim = kBN;
+      if (diag || kbase + kBN > N) {
+        lim = N - kbase;
+        if (diag && r + 1 < lim) lim = r + 1;  // key kbase + c visible iff c <= r
+      }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kBN; ++c) {
+        const float v = (c < lim) ? __uint_as_float(x[c]) * scale_log2 : -INFINITY;
+        x[c] = __float_as_uint(v);
+        mx = fmaxf(mx, v);
+      }
+      // Conditional rescale: keep the stale maximum unless it grew by more than 8
+      // (p <= 2^8 then); the decision is warp-uniform because TMEM access is.
+      float alpha = 1.0f;
+      bool rescale = false;
+      if (j == 0) {
+        m_run = mx;
+      } else {
+        const bool need = mx > m_run + 8.0f;
+        rescale = __any_sync(0xffffffffu, need);
+        if (need) {
+          alpha = ex2_approx(m_run - mx);
+          m_run = mx;
+        }
+      }
+      float rowsum = 0.f;
+#pragma unroll
+      for (int c = 0; c < kBN; c += 32) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float p0 = ex2_approx(__uint_as_float(x[c + 2 * e]) - m_run);
+          const float p1 = ex2_approx(__uint_as_float(x[c + 2 * e + 1]) - m_run);
+          rowsum += p0 + p1;
+          pk[e] = pack2<BF16>(p0, p1);
+        }
+        tmem_st16(tS + c / 2, pk);
+      }
+      l_run = l_run * alpha + rowsum;
+      if (rescale) {
+        // O_X was last written by PV_X(j-1), which completed before S_X(j) was issued.
+#pragma unroll
+        for (int c = 0; c < D; c += 32) {
+          uint32_t o[32];
+          tmem_ld32(tO + c, o);
+          tmem_ld_wait();
+          reg_fence<32>(o);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st32(tO + c, o);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar[BPFULL + X]);
+    }
+    if (ok && nX > 0) ok = __all_sync(0xffffffffu, mbar_wait(&bar[BODONE + X], (nX - 1) & 1,
+                                                             abort_flag, err));
+    if (ok && nX > 0) {
+      tc_fence_after();
+      const float inv_l = 1.0f / l_run;
+      const bool valid = q < N;
+      uint16_t* orow = reinterpret_cast<uint16_t*>(out) + (static_cast<size_t>(bh) * N + q) * D;
+#pragma unroll
+      for (int c = 0; c < D; c += 32) {
+        uint32_t o[32];
+        tmem_ld32(tO + c, o);
+        tmem_ld_wait();
+        reg_fence<32>(o);
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          pk[e] = pack2<BF16>(__uint_as_float(o[2 * e]) * inv_l, __uint_as_float(o[2 * e + 1]) * inv_l);
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c);
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4)
+            dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+        }
+      }
+      if (valid)
+        lse_out[static_cast<size_t>(bh) * N + q] = (m_run + log2f(l_run)) * 0.69314718055994530942f;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D, bool BF16>
+cudaError_t launch_fwd_t(const AttnShape& s, const FwdArgs& a, cudaStream_t stream) {
+  auto kern = fa_fwd_kernel<D, BF16>;
+  constexpr int smem = FwdSmem<D>::kAlloc;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const int T = (s.N + kBM - 1) / kBM;
+  const int pairs = (T + 1) / 2;
+  dim3 grid(static_cast<unsigned>(s.B * s.Hq), static_cast<unsigned>(pairs));
+  const float scale_log2 = s.scale * 1.4426950408889634f;
+  kern<<<grid, kThreads, smem, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.o, a.lse, s.Hq, s.Hkv, s.N,
+                                         s.causal, scale_log2, a.err);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t forward_smem_bytes(int d) {
+  return d == 64 ? FwdSmem<64>::kAlloc : FwdSmem<128>::kAlloc;
+}
+
+cudaError_t launch_forward(const AttnShape& s, const FwdArgs& a, cudaStream_t stream) {
+  if (s.d == 64) return s.bf16 ? launch_fwd_t<64, true>(s, a, stream) : launch_fwd_t<64, false>(s, a, stream);
+  return s.bf16 ? launch_fwd_t<128, true>(s, a, stream) : launch_fwd_t<128, false>(s, a, stream);
+}
+
+}  // namespace fa

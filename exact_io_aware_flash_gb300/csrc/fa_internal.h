@@ -1,0 +1,48 @@
+// Host-side interface between the C-ABI front end (fa_api.cu) and the kernel
+// translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace fa {
+
+struct AttnShape {
+  int B, Hq, Hkv, N, d;
+  int causal;
+  float scale;
+  int bf16;  // 1 = bfloat16, 0 = float16
+};
+
+// Tensor maps over [B*H, N, d] 16-bit tensors, box {64, 128, 1}, 128-byte swizzle.
+struct FwdArgs {
+  CUtensorMap tm_q, tm_k, tm_v;
+  void* o;
+  float* lse;
+  int* err;
+};
+
+struct BwdArgs {
+  CUtensorMap tm_q, tm_k, tm_v, tm_do;
+  const void* o;
+  const void* dO;
+  const float* lse;
+  float* D;       // [B*Hq*N]
+  float* dq_acc;  // [B*Hq*N*d]
+  void* dq;
+  void* dk;
+  void* dv;
+  int* err;
+};
+
+// Each returns cudaSuccess or the launch error.  `stream` is the caller's.
+cudaError_t launch_forward(const AttnShape& s, const FwdArgs& a, cudaStream_t stream);
+cudaError_t launch_backward(const AttnShape& s, const BwdArgs& a, cudaStream_t stream);
+
+// Shared-memory bytes the forward kernel needs for head dimension d (for checks).
+size_t forward_smem_bytes(int d);
+size_t backward_smem_bytes(int d);
+
+}  // namespace fa

@@ -1,0 +1,137 @@
+/*
+ * fa.h -- C ABI of libfa.so: exact IO-aware scaled-dot-product attention on
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The operation ("FlashAttention Primer: IO-Aware Attention, from FA1 to FA4",
+ * section "Why attention is quadratic", the SDPA equation; "Flash Attention"
+ * (aiwiki.ai), section "Definition and scope"):
+ *
+ *     S = scale * Q K^T,   P = rowsoftmax(S),   O = P V
+ *
+ * computed exactly (up to floating-point rounding order) by a tiled schedule
+ * that never writes S or P to device memory: the forward keeps a running row
+ * maximum and sum (online softmax, "FlashAttention Primer", section
+ * "FlashAttention-1"; "Flash Attention", section "Online softmax") and saves
+ * only O and the per-row log-sum-exp; the backward recomputes P block by block
+ * from that log-sum-exp ("FlashAttention Primer", section "Backward pass:
+ * recomputation instead of storage").
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - All tensor pointers are DEVICE pointers owned by the caller.  The library
+ *   never frees or keeps them beyond the call's stream work.
+ * - Layouts are dense row-major:
+ *     q, o, dO, dq : [B, Hq,  N, d]   (element type `dtype`)
+ *     k, v, dk, dv : [B, Hkv, N, d]   (element type `dtype`)
+ *     lse          : [B, Hq,  N]      (float32)
+ *   Every base pointer must be 16-byte aligned (the tiles are moved by the
+ *   Tensor Memory Accelerator, whose global addresses must be 16-byte aligned).
+ * - d must be 64 or 128.  N >= 1 (any value; ragged tails are masked).
+ *   Hq % Hkv == 0; query head h reads key/value head floor(h * Hkv / Hq)
+ *   (contiguous groups of Hq/Hkv query heads share one KV head).
+ * - causal != 0 masks key k for query i when k > i (square attention only).
+ * - scale multiplies Q K^T; pass 1/sqrt(d) for standard attention.  Any finite
+ *   value is accepted.
+ * - dtype: FA_DTYPE_FP16 or FA_DTYPE_BF16 (both operands and outputs).
+ * - stream: a cudaStream_t passed as void* (NULL = legacy default stream).
+ *   Every call only enqueues work on that stream and returns; it never
+ *   synchronises.  Calls on different streams may run concurrently.
+ * - Return value: FA_OK, or one of the FA_ERR_* codes below.  On any error
+ *   nothing has been enqueued and a message is available from fa_last_error()
+ *   on the same host thread.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Exported symbols keep default visibility even when the library is built with
+   -fvisibility=hidden. */
+#if defined(__GNUC__)
+#define FA_API __attribute__((visibility("default")))
+#else
+#define FA_API
+#endif
+
+#define FA_OK 0
+#define FA_ERR_INVALID 1     /* null pointer, non-positive size, Hq % Hkv != 0, non-finite scale,
+                                workspace too small */
+#define FA_ERR_UNSUPPORTED 2 /* d not in {64,128}, unknown dtype, misaligned pointer, size over
+                                the limits, device is not sm_103 */
+#define FA_ERR_CUDA 3        /* a CUDA runtime/driver call or a launch failed */
+#define FA_ERR_TIMEOUT 4     /* a kernel's bounded wait expired (reported by fa_check_errors) */
+
+#define FA_DTYPE_FP16 0
+#define FA_DTYPE_BF16 1
+
+/*
+ * Forward pass: O = softmax(scale * Q K^T) V and LSE.
+ *
+ * lse[b,h,i] = ln( sum_k exp(scale * q_i . k_k) ) over the visible keys k,
+ * the natural-log log-sum-exp of the scaled scores of row i ("FlashAttention
+ * Primer", section "Backward pass: recomputation instead of storage": the
+ * forward stores O and the per-row log-sum-exp, not the N x N matrix).
+ *
+ * Reads q, k, v; writes o and lse (every element with i < N).  Allocates
+ * nothing on the device.  Deterministic: the same inputs give bitwise the
+ * same outputs.
+ */
+FA_API int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+               int Hkv, int N, int d, int causal, float scale, int dtype, void* stream);
+
+/*
+ * Bytes of device workspace fa_backward needs for these sizes.  Returns 0 if
+ * the sizes are invalid.  Layout (offsets in bytes from the workspace base):
+ *   [0, a)        D      float32 [B, Hq, N], D_i = sum_c dO_ic * O_ic
+ *   [a, a + b)    dQacc  float32 [B, Hq, N, d], unscaled dQ accumulator
+ * with a = round_up(4*B*Hq*N, 256) and b = 4*B*Hq*N*d.
+ */
+FA_API size_t fa_backward_workspace_size(int B, int Hq, int N, int d);
+
+/*
+ * Backward pass from the saved statistics: given q, k, v, the forward's o and
+ * lse, and dO = dL/dO, writes dq, dk, dv (element type dtype).
+ *
+ * Steps, all on `stream`:
+ *   1. D_i = rowsum(dO_i * O_i) into the workspace, and zero dQacc;
+ *   2. per key/value tile, recompute P = exp(scale * Q K^T - LSE) block by
+ *      block, and accumulate dV += P^T dO, dS = P * (dO V^T - D),
+ *      dK += scale * dS^T Q (summed over the KV head's query group in the
+ *      kernel), dQacc += dS K (float32 atomic adds);
+ *   3. dq = scale * dQacc converted to dtype.
+ * The gradient is that of the definition: the primer's printed dS omits the
+ * -D term and the scale factor, which this library applies (the oracle's
+ * finite-difference checks fix the formula).
+ *
+ * workspace: device memory of at least fa_backward_workspace_size() bytes,
+ * 256-byte aligned, owned by the caller, not used concurrently by another
+ * call.  The dQ accumulation order varies between runs (atomic adds), so dq
+ * may differ in the last bits from run to run; dk and dv are deterministic.
+ */
+FA_API int fa_backward(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                const void* dO, void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
+                int B, int Hq, int Hkv, int N, int d, int causal, float scale, int dtype,
+                void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the device error word that the
+ * kernels set when a bounded wait expires.  Returns FA_OK, FA_ERR_TIMEOUT, or
+ * FA_ERR_CUDA if the synchronisation itself failed.
+ */
+FA_API int fa_check_errors(void* stream);
+
+/* Message for the last error returned on the calling host thread ("" if none). */
+FA_API const char* fa_last_error(void);
+
+/* Library version string. */
+FA_API const char* fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */
