@@ -65,6 +65,14 @@ int oracle_num_threads(void) {
 #endif
 }
 
+static int oracle_num_threads_in_team(void) {
+#ifdef _OPENMP
+    return omp_get_num_threads();
+#else
+    return 1;
+#endif
+}
+
 static double dot(const double* a, const double* b, int d) {
     double acc = 0.0;
     for (int c = 0; c < d; ++c) acc += a[c] * b[c];
@@ -136,8 +144,10 @@ int oracle_forward(const double* q, const double* k, const double* v, double* o,
 /*
  * Backward from the definition.  Recomputes P and O itself from (q, k, v); it
  * takes no forward output from anywhere else.  D (may be NULL) receives
- * D_i = dO_i . O_i.  Parallel over (b, kv-head) so that dK/dV of a KV head are
- * accumulated by one thread, summing its query-head group in order.
+ * D_i = dO_i . O_i.  KV heads are processed one after another; within one, the
+ * rows of its query-head group are spread over threads, each summing its rows'
+ * dK / dV contributions into a private buffer, and the buffers are added in
+ * thread order at the end (the definition's sums over rows are order-free).
  */
 int oracle_backward(const double* q, const double* k, const double* v, const double* dO,
                     double* dq, double* dk, double* dv, double* D, int B, int Hq,
@@ -147,67 +157,84 @@ int oracle_backward(const double* q, const double* k, const double* v, const dou
     if (!q || !k || !v || !dO || !dq || !dk || !dv) return ORACLE_EINVAL;
     const int group = Hq / Hkv;
     const int64_t heads = (int64_t)B * Hkv;
+    const size_t nd = (size_t)N * d;
     int failed = 0;
+    for (int64_t bg = 0; bg < heads && !failed; ++bg) {
+        const int64_t b = bg / Hkv;
+        const int g = (int)(bg % Hkv);
+        const double* kh = k + (size_t)bg * nd;
+        const double* vh = v + (size_t)bg * nd;
+        double* dkh = dk + (size_t)bg * nd;
+        double* dvh = dv + (size_t)bg * nd;
+        memset(dkh, 0, sizeof(double) * nd);
+        memset(dvh, 0, sizeof(double) * nd);
+        const int64_t rows = (int64_t)group * N;
 #pragma omp parallel
-    {
-        double* p = (double*)malloc(sizeof(double) * (size_t)N);
-        double* ds = (double*)malloc(sizeof(double) * (size_t)N);
-        double* oi = (double*)malloc(sizeof(double) * (size_t)d);
-        if (!p || !ds || !oi) {
+        {
+            double* p = (double*)malloc(sizeof(double) * (size_t)N);
+            double* ds = (double*)malloc(sizeof(double) * (size_t)N);
+            double* oi = (double*)malloc(sizeof(double) * (size_t)d);
+            double* dk_part = (double*)calloc(nd, sizeof(double));
+            double* dv_part = (double*)calloc(nd, sizeof(double));
+            const int ok = p && ds && oi && dk_part && dv_part;
+            if (!ok) {
 #pragma omp atomic write
-            failed = 1;
-        }
-#pragma omp for schedule(dynamic, 1)
-        for (int64_t bg = 0; bg < heads; ++bg) {
-            if (!p || !ds || !oi) continue;
-            const int64_t b = bg / Hkv;
-            const int g = (int)(bg % Hkv);
-            const double* kh = k + (size_t)bg * N * d;
-            const double* vh = v + (size_t)bg * N * d;
-            double* dkh = dk + (size_t)bg * N * d;
-            double* dvh = dv + (size_t)bg * N * d;
-            memset(dkh, 0, sizeof(double) * (size_t)N * d);
-            memset(dvh, 0, sizeof(double) * (size_t)N * d);
-            for (int hh = 0; hh < group; ++hh) {
+                failed = 1;
+            }
+#pragma omp for schedule(dynamic, 4)
+            for (int64_t r = 0; r < rows; ++r) {
+                if (!ok) continue;
+                const int hh = (int)(r / N);
+                const int i = (int)(r % N);
                 const int h = g * group + hh;
-                const size_t head = ((size_t)b * Hq + h) * (size_t)N;
-                for (int i = 0; i < N; ++i) {
-                    const double* qi = q + (head + i) * d;
-                    const double* doi = dO + (head + i) * d;
-                    double* dqi = dq + (head + i) * d;
-                    const int nk = causal ? i + 1 : N;
-                    softmax_row(qi, kh, nk, d, scale, p);
-                    /* O_i = sum_k P_ik v_k, then D_i = dO_i . O_i */
-                    for (int c = 0; c < d; ++c) oi[c] = 0.0;
-                    for (int kk = 0; kk < nk; ++kk)
-                        for (int c = 0; c < d; ++c) oi[c] += p[kk] * vh[(size_t)kk * d + c];
-                    const double Di = dot(doi, oi, d);
-                    if (D) D[head + i] = Di;
-                    /* dS_ik = P_ik (dO_i . v_k - D_i) */
-                    for (int kk = 0; kk < nk; ++kk)
-                        ds[kk] = p[kk] * (dot(doi, vh + (size_t)kk * d, d) - Di);
-                    /* dQ_i = scale sum_k dS_ik k_k */
-                    for (int c = 0; c < d; ++c) dqi[c] = 0.0;
-                    for (int kk = 0; kk < nk; ++kk)
-                        for (int c = 0; c < d; ++c) dqi[c] += ds[kk] * kh[(size_t)kk * d + c];
-                    for (int c = 0; c < d; ++c) dqi[c] *= scale;
-                    /* dK_k += scale dS_ik q_i ; dV_k += P_ik dO_i */
-                    for (int kk = 0; kk < nk; ++kk) {
-                        const double a = scale * ds[kk];
-                        const double w = p[kk];
-                        double* dkk = dkh + (size_t)kk * d;
-                        double* dvk = dvh + (size_t)kk * d;
-                        for (int c = 0; c < d; ++c) {
-                            dkk[c] += a * qi[c];
-                            dvk[c] += w * doi[c];
-                        }
+                const size_t row = ((size_t)b * Hq + h) * (size_t)N + i;
+                const double* qi = q + row * d;
+                const double* doi = dO + row * d;
+                double* dqi = dq + row * d;
+                const int nk = causal ? i + 1 : N;
+                softmax_row(qi, kh, nk, d, scale, p);
+                /* O_i = sum_k P_ik v_k, then D_i = dO_i . O_i */
+                for (int c = 0; c < d; ++c) oi[c] = 0.0;
+                for (int kk = 0; kk < nk; ++kk)
+                    for (int c = 0; c < d; ++c) oi[c] += p[kk] * vh[(size_t)kk * d + c];
+                const double Di = dot(doi, oi, d);
+                if (D) D[row] = Di;
+                /* dS_ik = P_ik (dO_i . v_k - D_i) */
+                for (int kk = 0; kk < nk; ++kk)
+                    ds[kk] = p[kk] * (dot(doi, vh + (size_t)kk * d, d) - Di);
+                /* dQ_i = scale sum_k dS_ik k_k */
+                for (int c = 0; c < d; ++c) dqi[c] = 0.0;
+                for (int kk = 0; kk < nk; ++kk)
+                    for (int c = 0; c < d; ++c) dqi[c] += ds[kk] * kh[(size_t)kk * d + c];
+                for (int c = 0; c < d; ++c) dqi[c] *= scale;
+                /* dK_k += scale dS_ik q_i ; dV_k += P_ik dO_i */
+                for (int kk = 0; kk < nk; ++kk) {
+                    const double a = scale * ds[kk];
+                    const double w = p[kk];
+                    double* dkk = dk_part + (size_t)kk * d;
+                    double* dvk = dv_part + (size_t)kk * d;
+                    for (int c = 0; c < d; ++c) {
+                        dkk[c] += a * qi[c];
+                        dvk[c] += w * doi[c];
                     }
                 }
             }
+#pragma omp for ordered schedule(static, 1)
+            for (int tt = 0; tt < oracle_num_threads_in_team(); ++tt) {
+#pragma omp ordered
+                if (ok) {
+                    for (size_t e = 0; e < nd; ++e) {
+                        dkh[e] += dk_part[e];
+                        dvh[e] += dv_part[e];
+                    }
+                }
+            }
+            free(p);
+            free(ds);
+            free(oi);
+            free(dk_part);
+            free(dv_part);
         }
-        free(p);
-        free(ds);
-        free(oi);
     }
     return failed ? ORACLE_ENOMEM : ORACLE_OK;
 }
