@@ -57,17 +57,35 @@ def test_forward_small_shapes(B, Hq, Hkv, N, d, causal, dtype):
     assert_matches(o, lse, o_ref, lse_ref, dtype, f"{shape} causal={causal}")
 
 
+UNIT_ROUNDOFF = {"fp16": 2.0 ** -11, "bf16": 2.0 ** -8}
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
 @pytest.mark.parametrize("q_scale,scale", [(8.0, None), (1.0, 0.0), (1.0, -0.3), (30.0, None)])
-def test_forward_score_ranges(q_scale, scale):
+def test_forward_score_ranges(q_scale, scale, dtype):
     """Large scores force the running maximum to move (rescaling path); zero and
-    negative scales exercise uniform attention and a reversed score order."""
+    negative scales exercise uniform attention and a reversed score order.
+
+    These inputs lie outside the evaluation workloads: with Q scaled up the
+    softmax is nearly one-hot and |O| approaches max|V|, so the flat O tolerance
+    no longer applies.  The bound used is the rounding of the arithmetic: P is
+    rounded to the 16-bit type before P V (relative error <= u per term, so
+    <= u * max|V| on the weighted sum) and O is rounded once on output (<= u|O|),
+    u the unit roundoff of the type; fp32 accumulation adds far less.
+    """
     shape = Shape(1, 2, 1, 700, 128)
-    inp = make_inputs(shape, "bf16", seed=99, with_dO=False, q_scale=q_scale)
+    inp = make_inputs(shape, dtype, seed=99, with_dO=False, q_scale=q_scale)
     s = 1.0 / math.sqrt(128) if scale is None else scale
+    u = UNIT_ROUNDOFF[dtype]
+    vmax = float(inp["v"].float().abs().max())
     for causal in (False, True):
         o, lse = gpu_forward(inp, causal, s)
         o_ref, lse_ref = oracle.forward(inp["q"], inp["k"], inp["v"], causal, s)
-        assert_matches(o, lse, o_ref, lse_ref, "bf16", f"q_scale={q_scale} scale={s} causal={causal}")
+        o_gpu = o.float().cpu().numpy()
+        bound = u * (np.abs(o_ref) + vmax) + 1e-4
+        worst = float((np.abs(o_gpu - o_ref) / bound).max())
+        assert worst <= 1.0, f"q_scale={q_scale} scale={s} causal={causal}: {worst:.3f} x bound"
+        assert np.abs(lse.cpu().numpy() - lse_ref).max() <= TOL_LSE
 
 
 def _run_workload(name, causal, heads):
