@@ -48,7 +48,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.fa_forward.restype = i
         lib.fa_backward_workspace_size.argtypes = [i, i, i, i]
         lib.fa_backward_workspace_size.restype = sz
-        lib.fa_backward.argtypes = [vp] * 10 + [sz] + [i] * 7 + [f, i, vp]
+        lib.fa_backward.argtypes = [vp] * 10 + [sz] + [i] * 6 + [f, i, vp]
         lib.fa_backward.restype = i
         lib.fa_check_errors.argtypes = [vp]
         lib.fa_check_errors.restype = i

@@ -21,8 +21,14 @@ TOL_REL = 1e-2
 
 
 def rel_fro(g, ref):
+    """Relative Frobenius error.  Where the exact gradient vanishes (a single key:
+    P = [1] so dS = 0 and dQ = dK = 0 exactly) the relative error is undefined;
+    there the error is measured against the unit scale of the N(0,1) inputs."""
     g = g.float().cpu().numpy() if isinstance(g, torch.Tensor) else g
-    return float(np.linalg.norm(g - ref) / max(np.linalg.norm(ref), 1e-30))
+    ref_norm = float(np.linalg.norm(ref))
+    if ref_norm < 1e-9:
+        return float(np.abs(g).max()) / 0.1  # <= 1e-2 means max |g| <= 1e-3
+    return float(np.linalg.norm(g - ref) / ref_norm)
 
 
 def gpu_fwd_bwd(inp, causal, scale, workspace=None):
@@ -84,10 +90,7 @@ def test_backward_score_ranges(q_scale):
         _, _, dq, dk, dv = gpu_fwd_bwd(inp, causal, scale)
         dq_r, dk_r, dv_r, _ = oracle.backward(inp["q"], inp["k"], inp["v"], inp["dO"], causal, scale)
         for name, g, r in (("dq", dq, dq_r), ("dk", dk, dk_r), ("dv", dv, dv_r)):
-            if np.linalg.norm(r) < 1e-6:  # dK is exactly 0 when Q = 0
-                assert float(g.float().abs().max()) <= 1e-3
-                continue
-            assert rel_fro(g, r) <= TOL_REL, (name, causal, q_scale)
+            assert rel_fro(g, r) <= TOL_REL, (name, causal, q_scale)  # dK = 0 exactly for Q = 0
 
 
 def test_dk_dv_are_deterministic():
