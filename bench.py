@@ -1,0 +1,463 @@
+#!/usr/bin/env python
+"""Benchmark: one step = the whole attention hot path (fa_forward + fa_backward)
+on one batch of synthetic input, timed on the GPU with CUDA events.
+
+Workload: B=8, H=16 (Hq = Hkv), N=4096, d=128, bf16, causal, scale 1/sqrt(d),
+Q/K/V/dO iid N(0,1) -- the N=4096 point of the backward sweep (B*N = 32768),
+run forward then backward as in a training step.  Each of Q, K, V, O, dO is
+134 MB, larger than the 129 MB L2, so no L2 flush is needed between steps.
+
+Metric: attention fwd+bwd TFLOPS, algorithmic FLOPs (forward 4*B*H*N^2*d halved
+for causal, backward 2.5x that) divided by device time.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--sweep]
+
+With torchrun (N>1) every rank runs its own replica of the workload (the op has
+no cross-GPU exchange) and rank 0 prints the whole-job throughput.
+`--impl reference` times the fp64 CPU oracle (the only reference available) on
+a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import glob
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd/bwd TFLOPS at N=1k–16k, d=128 bf16; % of GB300 tensor peak"
+WORKLOAD = dict(B=8, Hq=16, Hkv=16, N=4096, d=128, causal=True, dtype="bf16", seed=1005 + 4096)
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def workload_config():
+    w = WORKLOAD
+    return {
+        "workload": f"attention fwd+bwd B{w['B']} H{w['Hq']} N{w['N']} d{w['d']} {w['dtype']} causal "
+                    "(backward-sweep point N=4096, B*N=32768)",
+        "B": w["B"], "Hq": w["Hq"], "Hkv": w["Hkv"], "N": w["N"], "d": w["d"],
+        "causal": w["causal"], "scale": "1/sqrt(d)",
+        "l2": "no flush: each of Q, K, V, O, dO (134 MB) is larger than the 129 MB L2",
+    }
+
+
+def flops_per_step():
+    from exact_io_aware_flash_gb300.flops import backward_flops, forward_flops
+
+    w = WORKLOAD
+    f = forward_flops(w["B"], w["Hq"], w["N"], w["d"], w["causal"])
+    b = backward_flops(w["B"], w["Hq"], w["N"], w["d"], w["causal"])
+    return f, b
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def start(self):
+        os.makedirs(os.path.dirname(self.path), exist_ok=True)
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ traffic
+def kernel_sources_digest() -> str:
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "exact_io_aware_flash_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(os.path.basename(p).encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, or None if the
+    kernel sources changed since those counters were taken."""
+    p = os.path.join(ROOT, "profiles", f"{kernel}_dram.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("sources_digest") != kernel_sources_digest():
+        return None
+    return d.get("dram_bytes_per_launch_full_workload")
+
+
+# ------------------------------------------------------------------ CPU oracle
+def cpu_oracle_sample(budget_s: float, max_heads: int):
+    """Time the fp64 oracle (as it stands) on whole heads of the workload until
+    `budget_s` seconds of CPU work; returns (flops, seconds, heads, threads)."""
+    import oracle
+    from exact_io_aware_flash_gb300.flops import backward_flops, forward_flops
+    from exact_io_aware_flash_gb300.synth import Shape, make_inputs
+
+    w = WORKLOAD
+    inp = make_inputs(Shape(1, 1, 1, w["N"], w["d"]), w["dtype"], seed=w["seed"])
+    scale = 1.0 / math.sqrt(w["d"])
+    per_head = forward_flops(1, 1, w["N"], w["d"], True) + backward_flops(1, 1, w["N"], w["d"], True)
+    oracle.build()
+    heads, t_total = 0, 0.0
+    while heads < max_heads and (heads == 0 or t_total < budget_s):
+        t0 = time.perf_counter()
+        oracle.forward(inp["q"], inp["k"], inp["v"], True, scale)
+        oracle.backward(inp["q"], inp["k"], inp["v"], inp["dO"], True, scale)
+        t_total += time.perf_counter() - t0
+        heads += 1
+    return per_head * heads, t_total, heads, oracle.num_threads()
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import oracle
+    from exact_io_aware_flash_gb300.flops import backward_flops, forward_flops
+    from exact_io_aware_flash_gb300.synth import Shape, make_inputs
+
+    w = WORKLOAD
+    oracle.build()
+    scale = 1.0 / math.sqrt(w["d"])
+    # Bounded sample per step: one head's causal prefix of n tokens (the first n
+    # queries of a causal head attend only to the first n keys, so the prefix is
+    # itself a complete causal attention problem).  n is sized so the whole run
+    # stays within about three minutes.
+    total_budget = 180.0
+    per_step_budget = min(4.0, total_budget / max(1, args.steps + args.warmup))
+    inp_full = make_inputs(Shape(1, 1, 1, w["N"], w["d"]), w["dtype"], seed=w["seed"])
+
+    def step(n):
+        sl = lambda t: t[:, :, :n].contiguous()
+        oracle.forward(sl(inp_full["q"]), sl(inp_full["k"]), sl(inp_full["v"]), True, scale)
+        oracle.backward(sl(inp_full["q"]), sl(inp_full["k"]), sl(inp_full["v"]), sl(inp_full["dO"]),
+                        True, scale)
+
+    def step_flops(n):
+        return forward_flops(1, 1, n, w["d"], True) + backward_flops(1, 1, n, w["d"], True)
+
+    t0 = time.perf_counter()
+    step(512)
+    rate = step_flops(512) / max(time.perf_counter() - t0, 1e-6)
+    n = 512
+    while n * 2 <= w["N"] and step_flops(n * 2) / rate <= per_step_budget:
+        n *= 2
+    for _ in range(args.warmup):
+        step(n)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step(n)
+    dt = time.perf_counter() - t0
+    value = step_flops(n) * args.steps / dt / 1e12
+    sample = (f"per step: one head (b=0, h=0) of the workload, causal prefix of {n} of {w['N']} "
+              f"tokens, fp64 forward + backward")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": workload_config(),
+        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from exact_io_aware_flash_gb300 import build as fa_build
+
+    fa_build.build()
+    from exact_io_aware_flash_gb300 import (backward, check_errors, forward,
+                                            set_backward_event_hooks, workspace_size)
+    from exact_io_aware_flash_gb300.synth import Shape, make_inputs
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+
+    w = WORKLOAD
+    shape = Shape(w["B"], w["Hq"], w["Hkv"], w["N"], w["d"])
+    inp = make_inputs(shape, w["dtype"], seed=w["seed"] + rank)
+    q, k, v, dO = (inp[n].to(dev) for n in ("q", "k", "v", "dO"))
+    scale = 1.0 / math.sqrt(w["d"])
+    o = torch.empty_like(q)
+    lse = torch.empty(w["B"], w["Hq"], w["N"], dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(workspace_size(w["B"], w["Hq"], w["N"], w["d"]), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        forward(q, k, v, causal=True, scale=scale, out=o, lse=lse)
+        if ev is not None:
+            ev[1].record(stream)
+        backward(q, k, v, o, lse, dO, causal=True, scale=scale, dq=dq, dk=dk, dv=dv, workspace=ws)
+        if ev is not None:
+            ev[4].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    check_errors()
+    if world > 1:
+        dist.barrier()
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    for e in evs:  # create the CUDA handles before the timed region
+        for x in e:
+            x.record(stream)
+    torch.cuda.synchronize()
+
+    gpu_id = str(local_rank)
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid) \
+            if not str(torch.cuda.get_device_properties(dev).uuid).startswith("GPU-") \
+            else str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(gpu_id)
+    sampler.start()
+    time.sleep(0.3)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    start.record(stream)
+    for i in range(K):
+        set_backward_event_hooks(evs[i][2], evs[i][3])
+        step(evs[i])
+    end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    set_backward_event_hooks(None, None)
+    clocks = sampler.stop()
+    check_errors()
+
+    elapsed_ms = start.elapsed_time(end)
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    bwd_ms = statistics.mean(e[1].elapsed_time(e[4]) for e in evs)
+    bwd_main_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+
+    f_fwd, f_bwd = flops_per_step()
+    value = world * (f_fwd + f_bwd) * K / (elapsed_ms * 1e-3) / 1e12
+
+    # end-to-end through the public API with pinned host buffers: H2D of the
+    # step's inputs, forward, backward, D2H of the gradients, every step.
+    host = {n: inp[n].pin_memory() for n in ("q", "k", "v", "dO")}
+    out_h = {n: torch.empty(t.shape, dtype=t.dtype).pin_memory() for n, t in (("dq", dq), ("dk", dk), ("dv", dv))}
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in out_h.values())
+    E = max(3, min(K, 20))
+
+    def e2e_step():
+        q.copy_(host["q"], non_blocking=True)
+        k.copy_(host["k"], non_blocking=True)
+        v.copy_(host["v"], non_blocking=True)
+        dO.copy_(host["dO"], non_blocking=True)
+        step()
+        out_h["dq"].copy_(dq, non_blocking=True)
+        out_h["dk"].copy_(dk, non_blocking=True)
+        out_h["dv"].copy_(dv, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(E):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    check_errors()
+    e2e_value = world * (f_fwd + f_bwd) * E / (e2e_ms * 1e-3) / 1e12
+
+    if rank == 0:
+        peaks, peak_kind = load_peaks()
+        peak = peaks["bf16_tflops_sustained"]
+        achieved = f_bwd / (bwd_main_ms * 1e-3) / 1e12
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": elapsed_ms / K, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic: Q, K, V, dO iid N(0,1) fp32 rounded to bf16, seeded",
+            "config": workload_config(),
+            "pct_of_bf16_peak": {"burst": value / world / peaks["bf16_tflops"],
+                                 "sustained": value / world / peaks["bf16_tflops_sustained"],
+                                 "peaks": peak_kind},
+            "components": {
+                "forward": {"ms": fwd_ms, "tflops": f_fwd / (fwd_ms * 1e-3) / 1e12,
+                            "kernel": "fa_fwd_kernel"},
+                "backward": {"ms": bwd_ms, "tflops": f_bwd / (bwd_ms * 1e-3) / 1e12,
+                             "main_kernel_ms": bwd_main_ms,
+                             "kernels": ["fa_bwd_pre_kernel", "fa_bwd_kernel", "fa_bwd_dq_kernel"]},
+            },
+            "roofline": {
+                "kernel": "fa_bwd_kernel", "bound": "tensor", "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak,
+                "peak_kind": f"{peak_kind} bf16 sustained (kernel timed inside a long step)",
+                "frac_of_burst": achieved / peaks["bf16_tflops"],
+                "traffic": recorded_traffic("fa_bwd_kernel"),
+                "algorithmic": "2.5 * 4*B*H*N^2*d / 2 FLOPs per launch (five N x N x d products, causal)",
+            },
+            "clocks": clocks,
+            "e2e": {"value": e2e_value, "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": E},
+            "gpu_launches": 4 * K,
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            fl, secs, heads, threads = cpu_oracle_sample(budget_s=12.0, max_heads=16)
+            line["cpu_baseline"] = {
+                "value": fl / secs / 1e12, "unit": "TFLOPS", "cores": threads, "kind": "oracle",
+                "sample": f"{heads} full head(s) (b=0, h=0 inputs) of the workload, N={WORKLOAD['N']}, "
+                          f"fp64 forward + backward, {secs:.1f} s"}
+        print(json.dumps(line), flush=True)
+        if args.sweep:
+            sweep(dev)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def sweep(dev):
+    """Extra lines (not the bench line): forward workloads and the backward sweep."""
+    import torch
+
+    from exact_io_aware_flash_gb300 import backward, check_errors, forward, workspace_size
+    from exact_io_aware_flash_gb300.flops import backward_flops, forward_flops
+    from exact_io_aware_flash_gb300.synth import (BACKWARD_SWEEP_N, WORKLOADS, backward_sweep_shape,
+                                                  make_inputs)
+
+    def timed(fn, iters=20):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(iters):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        check_errors()
+        return a.elapsed_time(b) / iters
+
+    for name, wl in WORKLOADS.items():
+        s = wl["shape"]
+        inp = make_inputs(s, wl["dtype"], seed=wl["seed"], with_dO=False)
+        q, k, v = (inp[n].to(dev) for n in ("q", "k", "v"))
+        for causal in wl["causal"]:
+            ms = timed(lambda: forward(q, k, v, causal=causal))
+            fl = forward_flops(s.B, s.Hq, s.N, s.d, causal)
+            print(json.dumps({"sweep": "forward", "workload": name, "causal": causal, "ms": ms,
+                              "tflops": fl / ms / 1e9}), flush=True)
+    for N in BACKWARD_SWEEP_N:
+        s = backward_sweep_shape(N)
+        inp = make_inputs(s, "bf16", seed=1005 + N)
+        q, k, v, dO = (inp[n].to(dev) for n in ("q", "k", "v", "dO"))
+        o, lse = forward(q, k, v, causal=True)
+        ws = torch.empty(workspace_size(s.B, s.Hq, s.N, s.d), dtype=torch.uint8, device=dev)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        ms = timed(lambda: backward(q, k, v, o, lse, dO, causal=True, dq=dq, dk=dk, dv=dv,
+                                    workspace=ws), iters=10)
+        fl = backward_flops(s.B, s.Hq, s.N, s.d, True)
+        print(json.dumps({"sweep": "backward", "B": s.B, "H": s.Hq, "N": N, "d": 128,
+                          "ms": ms, "tflops": fl / ms / 1e9}), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--sweep", action="store_true", help="also print per-workload lines")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -50,6 +50,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.fa_backward_workspace_size.restype = sz
         lib.fa_backward.argtypes = [vp] * 10 + [sz] + [i] * 6 + [f, i, vp]
         lib.fa_backward.restype = i
+        lib.fa_set_backward_event_hooks.argtypes = [vp, vp]
+        lib.fa_set_backward_event_hooks.restype = i
         lib.fa_check_errors.argtypes = [vp]
         lib.fa_check_errors.restype = i
         lib.fa_last_error.argtypes = []
@@ -153,6 +155,17 @@ def backward(q, k, v, o, lse, dO, causal: bool = False, scale: float | None = No
                             _stream_handle(stream))
     _raise(rc)
     return dq, dk, dv
+
+
+def set_backward_event_hooks(before=None, after=None) -> None:
+    """Record CUDA events around the backward's main kernel (see fa.h); None, None stops.
+
+    ``before`` / ``after`` are torch.cuda.Event objects that have been recorded
+    at least once (so their CUDA handles exist).
+    """
+    hb = None if before is None else before.cuda_event
+    ha = None if after is None else after.cuda_event
+    _raise(load().fa_set_backward_event_hooks(hb, ha))
 
 
 def check_errors(stream=None) -> None:

@@ -18,6 +18,8 @@ namespace {
 __device__ int g_fa_error_word;
 
 thread_local std::string t_last_error;
+thread_local cudaEvent_t t_ev_before = nullptr;
+thread_local cudaEvent_t t_ev_after = nullptr;
 
 int fail(int code, const char* fmt, ...) {
   char buf[512];
@@ -199,8 +201,19 @@ int fa_backward(const void* q, const void* k, const void* v, const void* o, cons
   a.dk = dk;
   a.dv = dv;
   a.err = st->err_word;
+  a.ev_before_main = t_ev_before;
+  a.ev_after_main = t_ev_after;
   cudaError_t e = fa::launch_backward(s, a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(FA_ERR_CUDA, "backward launch: %s", cudaGetErrorString(e));
+  return FA_OK;
+}
+
+int fa_set_backward_event_hooks(void* before, void* after) {
+  t_last_error.clear();
+  if ((before == nullptr) != (after == nullptr))
+    return fail(FA_ERR_INVALID, "pass both events or neither");
+  t_ev_before = static_cast<cudaEvent_t>(before);
+  t_ev_after = static_cast<cudaEvent_t>(after);
   return FA_OK;
 }
 

@@ -113,11 +113,6 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
-// Named barrier for one warpgroup (ids 1 and 2; 0 is __syncthreads).
-__device__ __forceinline__ void wg_sync(int id) {
-  asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory");
-}
-
 // ------------------------------------------------------------------ preprocessing
 // D_i = sum_c dO_ic O_ic (fp32) and dQacc = 0.  D/8 threads per row, 16 bytes each.
 template <int D, bool BF16>
@@ -510,10 +505,12 @@ cudaError_t launch_bwd_t(const AttnShape& s, const BwdArgs& a, cudaStream_t stre
   if (e != cudaSuccess) return e;
   const int T = (s.N + kBlk - 1) / kBlk;
   dim3 grid(static_cast<unsigned>(s.B * s.Hkv), static_cast<unsigned>(T));
+  if (a.ev_before_main && (e = cudaEventRecord(a.ev_before_main, stream)) != cudaSuccess) return e;
   kern<<<grid, kThreads, smem, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.lse, a.D, a.dq_acc,
                                          a.dk, a.dv, s.Hq, s.Hkv, s.N, s.causal, s.scale, a.err);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  if (a.ev_after_main && (e = cudaEventRecord(a.ev_after_main, stream)) != cudaSuccess) return e;
 
   const long n8 = rows * D / 8;
   fa_bwd_dq_kernel<BF16><<<grid_for(n8, 256), 256, 0, stream>>>(

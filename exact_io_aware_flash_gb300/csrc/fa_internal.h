@@ -35,6 +35,8 @@ struct BwdArgs {
   void* dk;
   void* dv;
   int* err;
+  cudaEvent_t ev_before_main;  // may be null: recorded around the main kernel
+  cudaEvent_t ev_after_main;
 };
 
 // Each returns cudaSuccess or the launch error.  `stream` is the caller's.

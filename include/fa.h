@@ -118,6 +118,17 @@ FA_API int fa_backward(const void* q, const void* k, const void* v, const void* 
                 void* stream);
 
 /*
+ * Profiling hook for the backward's main kernel.  After this call, every
+ * fa_backward issued from the calling host thread records `before` on its stream
+ * immediately before launching the main (recomputing) kernel and `after`
+ * immediately after it, so cudaEventElapsedTime(before, after) is that kernel's
+ * device time.  Both are cudaEvent_t handles passed as void*, created and owned
+ * by the caller; pass NULL, NULL to stop.  Thread-local; never synchronises.
+ * Returns FA_OK, or FA_ERR_INVALID if exactly one of the two is NULL.
+ */
+FA_API int fa_set_backward_event_hooks(void* before, void* after);
+
+/*
  * Synchronises `stream`, then reads and clears the device error word that the
  * kernels set when a bounded wait expires.  Returns FA_OK, FA_ERR_TIMEOUT, or
  * FA_ERR_CUDA if the synchronisation itself failed.
