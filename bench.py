@@ -21,7 +21,6 @@ from __future__ import annotations
 
 import argparse
 import hashlib
-import glob
 import json
 import math
 import os
@@ -119,23 +118,27 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ traffic
-def kernel_sources_digest() -> str:
+KERNEL_SOURCES = {"fa_bwd_kernel": ("fa_bwd.cu", "ptx.cuh"), "fa_fwd_kernel": ("fa_fwd.cu", "ptx.cuh")}
+
+
+def kernel_sources_digest(kernel: str) -> str:
+    """Digest of the source files that define `kernel`."""
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "exact_io_aware_flash_gb300", "csrc", "*"))):
-        with open(p, "rb") as f:
-            h.update(os.path.basename(p).encode() + f.read())
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "exact_io_aware_flash_gb300", "csrc", name), "rb") as f:
+            h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic(kernel: str):
     """DRAM bytes per launch from the committed ncu summary, or None if the
-    kernel sources changed since those counters were taken."""
+    kernel's sources changed since those counters were taken."""
     p = os.path.join(ROOT, "profiles", f"{kernel}_dram.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
-    if d.get("sources_digest") != kernel_sources_digest():
+    if d.get("sources_digest") != kernel_sources_digest(kernel):
         return None
     return d.get("dram_bytes_per_launch_full_workload")
 
@@ -384,7 +387,7 @@ def run_ours(args):
             "gpu_launches": 4 * K,
         }
         if world == 1 and not args.no_cpu_baseline:
-            fl, secs, heads, threads = cpu_oracle_sample(budget_s=12.0, max_heads=16)
+            fl, secs, heads, threads = cpu_oracle_sample(budget_s=12.0, max_heads=64)
             line["cpu_baseline"] = {
                 "value": fl / secs / 1e12, "unit": "TFLOPS", "cores": threads, "kind": "oracle",
                 "sample": f"{heads} full head(s) (b=0, h=0 inputs) of the workload, N={WORKLOAD['N']}, "
