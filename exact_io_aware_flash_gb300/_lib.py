@@ -50,6 +50,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.fa_backward_workspace_size.restype = sz
         lib.fa_backward.argtypes = [vp] * 10 + [sz] + [i] * 6 + [f, i, vp]
         lib.fa_backward.restype = i
+        lib.fa_backward_noalloc.argtypes = [vp] * 9 + [i] * 6 + [f, i, vp]
+        lib.fa_backward_noalloc.restype = i
         lib.fa_set_backward_event_hooks.argtypes = [vp, vp]
         lib.fa_set_backward_event_hooks.restype = i
         lib.fa_check_errors.argtypes = [vp]

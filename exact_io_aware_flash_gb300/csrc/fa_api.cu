@@ -131,6 +131,20 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 }  // namespace
 
+namespace fa {
+
+int set_last_error(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+  return code;
+}
+
+}  // namespace fa
+
 extern "C" {
 
 const char* fa_version(void) { return "fa-gb300 0.1.0 (sm_103a, tcgen05/TMEM/TMA)"; }

@@ -43,6 +43,9 @@ struct BwdArgs {
 cudaError_t launch_forward(const AttnShape& s, const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_backward(const AttnShape& s, const BwdArgs& a, cudaStream_t stream);
 
+// Records `fmt` as the calling thread's fa_last_error() message; returns `code`.
+int set_last_error(int code, const char* fmt, ...);
+
 // Shared-memory bytes the forward kernel needs for head dimension d (for checks).
 size_t forward_smem_bytes(int d);
 size_t backward_smem_bytes(int d);

@@ -118,6 +118,39 @@ FA_API int fa_backward(const void* q, const void* k, const void* v, const void* 
                 void* stream);
 
 /*
+ * Backward pass that allocates nothing.  (Library-side addition: the attention
+ * method has no counterpart of it.)
+ *
+ * Same arguments, outputs, errors and asynchrony as fa_backward, minus the
+ * workspace: the scratch fa_backward needs (the D vector and the float32 dQ
+ * accumulator, fa_backward_workspace_size() bytes) is taken from one
+ * FA_NOALLOC_SCRATCH_BYTES-byte array compiled into the library's device code,
+ * which every GPU that loads the library holds until the process exits.  It is
+ * for callers that may not call cudaMalloc or any other allocator: a host
+ * program that reserves all device memory up front and forbids allocation
+ * afterwards, a plugin running inside a framework that gives it no allocator,
+ * or a latency-critical loop that cannot afford an allocation's implicit
+ * device synchronisation.  The caller still provides every input and output.
+ *
+ * - Sizes whose fa_backward_workspace_size() exceeds FA_NOALLOC_SCRATCH_BYTES
+ *   are rejected with FA_ERR_UNSUPPORTED (nothing is enqueued); use
+ *   fa_backward with a workspace for those.
+ * - The first call on each device looks up the array's device address with
+ *   that device current; make that first call before any stream capture.
+ * - Every call on a device shares the one array and leaves its contents
+ *   behind; each call clears what must start at zero (the dQ accumulator) and
+ *   overwrites the rest.  Calls whose GPU work overlaps (different streams, or
+ *   different host threads, without ordering between them) race on the array
+ *   and give wrong gradients: serialise them.
+ * - Calls no cudaMalloc, cudaFree or other allocating routine.
+ */
+#define FA_NOALLOC_SCRATCH_BYTES (40 * 1024 * 1024)
+FA_API int fa_backward_noalloc(const void* q, const void* k, const void* v, const void* o,
+                               const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                               int B, int Hq, int Hkv, int N, int d, int causal, float scale,
+                               int dtype, void* stream);
+
+/*
  * Profiling hook for the backward's main kernel.  After this call, every
  * fa_backward issued from the calling host thread records `before` on its stream
  * immediately before launching the main (recomputing) kernel and `after`

@@ -1,0 +1,73 @@
+"""fa_backward_noalloc against fa_backward, through the C ABI.
+
+fa_backward_noalloc serves callers that may not allocate device memory: it
+takes its scratch from an array built into the library instead of a
+caller-provided workspace.  Its gradients must match those of the workspace
+entry point within the backward parity tolerance (relative Frobenius error
+<= 1e-2), on two calls in a row (the second call reuses the array the first
+one left behind, so anything that must start at zero has to be cleared).
+
+This file is named so that pytest collects it last.
+"""
+import ctypes
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from exact_io_aware_flash_gb300 import _lib, backward, build, check_errors, forward
+from exact_io_aware_flash_gb300.synth import Shape, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+TOL_REL = 1e-2
+
+
+def _rel(a, b):
+    a = a.float().cpu().numpy()
+    b = b.float().cpu().numpy()
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
+
+
+def _noalloc(lib, q, k, v, o, lse, dO, causal, scale):
+    B, Hq, N, d = q.shape
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    rc = lib.fa_backward_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                 lse.data_ptr(), dO.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                 dv.data_ptr(), B, Hq, k.shape[1], N, d, int(causal), scale,
+                                 _lib.FA_DTYPE_BF16, torch.cuda.current_stream().cuda_stream)
+    assert rc == 0, lib.fa_last_error().decode()
+    return dq, dk, dv
+
+
+def test_noalloc_backward_matches_workspace_backward_twice():
+    build.build()
+    lib = _lib.load()
+    shape = Shape(2, 8, 2, 1000, 128)
+    inp = make_inputs(shape, "bf16", seed=4242)
+    q, k, v, dO = (inp[n].cuda() for n in ("q", "k", "v", "dO"))
+    scale = 1.0 / math.sqrt(128)
+    o, lse = forward(q, k, v, causal=True, scale=scale)
+    ref = backward(q, k, v, o, lse, dO, causal=True, scale=scale)
+    check_errors()
+    for call in range(2):
+        got = _noalloc(lib, q, k, v, o, lse, dO, True, scale)
+        torch.cuda.synchronize()
+        check_errors()
+        for name, g, r in zip(("dq", "dk", "dv"), got, ref):
+            e = _rel(g, r)
+            assert e <= TOL_REL, f"call {call}: {name} relative error {e:.3g}"
+
+
+def test_noalloc_rejects_sizes_beyond_its_scratch():
+    build.build()
+    lib = _lib.load()
+    # B*Hq*N*d*4 bytes of dQ accumulator alone exceeds the 40 MiB array.
+    B, Hq, N, d = 4, 16, 4096, 128
+    assert lib.fa_backward_workspace_size(B, Hq, N, d) > 40 * 1024 * 1024
+    fake = ctypes.c_void_p(4096)  # rejected before any pointer is used
+    rc = lib.fa_backward_noalloc(fake, fake, fake, fake, fake, fake, fake, fake, fake,
+                                 B, Hq, Hq, N, d, 1, 0.1, _lib.FA_DTYPE_BF16, None)
+    assert rc == _lib.FA_ERR_UNSUPPORTED
+    assert b"scratch" in lib.fa_last_error()
