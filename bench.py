@@ -118,7 +118,9 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ traffic
-KERNEL_SOURCES = {"fa_bwd_kernel": ("fa_bwd.cu", "ptx.cuh"), "fa_fwd_kernel": ("fa_fwd.cu", "ptx.cuh")}
+KERNEL_SOURCES = {"fa_bwd_dkdv_kernel": ("fa_bwd.cu", "ptx.cuh"),
+                  "fa_bwd_dq_kernel": ("fa_bwd.cu", "ptx.cuh"),
+                  "fa_fwd_kernel": ("fa_fwd.cu", "ptx.cuh")}
 
 
 def kernel_sources_digest(kernel: str) -> str:
@@ -263,7 +265,7 @@ def run_ours(args):
             ev[1].record(stream)
         backward(q, k, v, o, lse, dO, causal=True, scale=scale, dq=dq, dk=dk, dv=dv, workspace=ws)
         if ev is not None:
-            ev[4].record(stream)
+            ev[5].record(stream)
 
     for _ in range(args.warmup):
         step()
@@ -273,7 +275,9 @@ def run_ours(args):
         dist.barrier()
 
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    # per step: before/after the forward, before the dK/dV kernel, before the
+    # dQ kernel, after the dQ kernel (recorded by the library), after the backward
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
     for e in evs:  # create the CUDA handles before the timed region
         for x in e:
             x.record(stream)
@@ -295,13 +299,13 @@ def run_ours(args):
         dist.barrier()
     start.record(stream)
     for i in range(K):
-        set_backward_event_hooks(evs[i][2], evs[i][3])
+        set_backward_event_hooks(evs[i][2], evs[i][3], evs[i][4])
         step(evs[i])
     end.record(stream)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    set_backward_event_hooks(None, None)
+    set_backward_event_hooks(None, None, None)
     clocks = sampler.stop()
     check_errors()
 
@@ -311,8 +315,9 @@ def run_ours(args):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         elapsed_ms = float(t.item())
     fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
-    bwd_ms = statistics.mean(e[1].elapsed_time(e[4]) for e in evs)
-    bwd_main_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+    bwd_ms = statistics.mean(e[1].elapsed_time(e[5]) for e in evs)
+    dkdv_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+    dq_ms = statistics.mean(e[3].elapsed_time(e[4]) for e in evs)
 
     f_fwd, f_bwd = flops_per_step()
     value = world * (f_fwd + f_bwd) * K / (elapsed_ms * 1e-3) / 1e12
@@ -356,7 +361,19 @@ def run_ours(args):
     if rank == 0:
         peaks, peak_kind = load_peaks()
         peak = peaks["bf16_tflops_sustained"]
-        achieved = f_bwd / (bwd_main_ms * 1e-3) / 1e12
+        # Algorithmic FLOPs of each kernel: the N x N x d products it performs
+        # (forward 2: S, PV; dK/dV 4: S^T, dP^T, dV, dK; dQ 3: S, dP, dQ), each
+        # 2*B*H*N^2*d halved for causal.
+        per_product = f_fwd / 2.0
+        kernels = {
+            "fa_fwd_kernel": (fwd_ms, 2 * per_product, "2 products: S = Q K^T, O += P V"),
+            "fa_bwd_dkdv_kernel": (dkdv_ms, 4 * per_product,
+                                   "4 products: S^T, dP^T, dV += P^T dO, dK += dS^T Q"),
+            "fa_bwd_dq_kernel": (dq_ms, 3 * per_product, "3 products: S, dP, dQ += dS K"),
+        }
+        dom = max(kernels, key=lambda k: kernels[k][0])
+        dom_ms, dom_flops, dom_what = kernels[dom]
+        achieved = dom_flops / (dom_ms * 1e-3) / 1e12
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": elapsed_ms / K, "higher_is_better": True,
@@ -370,16 +387,20 @@ def run_ours(args):
                 "forward": {"ms": fwd_ms, "tflops": f_fwd / (fwd_ms * 1e-3) / 1e12,
                             "kernel": "fa_fwd_kernel"},
                 "backward": {"ms": bwd_ms, "tflops": f_bwd / (bwd_ms * 1e-3) / 1e12,
-                             "main_kernel_ms": bwd_main_ms,
-                             "kernels": ["fa_bwd_pre_kernel", "fa_bwd_kernel", "fa_bwd_dq_kernel"]},
+                             "dkdv_kernel_ms": dkdv_ms, "dq_kernel_ms": dq_ms,
+                             "kernels": ["fa_bwd_pre_kernel", "fa_bwd_dkdv_kernel", "fa_bwd_dq_kernel"],
+                             "note": "TFLOPS counts the 5 products of the gradient; the kernels "
+                                     "recompute S and dP in both passes (7 products)"},
             },
             "roofline": {
-                "kernel": "fa_bwd_kernel", "bound": "tensor", "achieved": achieved, "peak": peak,
+                "kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak,
                 "unit": "TFLOP/s", "frac": achieved / peak,
                 "peak_kind": f"{peak_kind} bf16 sustained (kernel timed inside a long step)",
                 "frac_of_burst": achieved / peaks["bf16_tflops"],
-                "traffic": recorded_traffic("fa_bwd_kernel"),
-                "algorithmic": "2.5 * 4*B*H*N^2*d / 2 FLOPs per launch (five N x N x d products, causal)",
+                "traffic": recorded_traffic(dom),
+                "algorithmic": f"{dom_what}; each 2*B*H*N^2*d/2 FLOPs (causal); "
+                               f"{dom_flops / 1e9:.1f} GFLOP per launch",
+                "per_kernel_tflops": {k: v[1] / (v[0] * 1e-3) / 1e12 for k, v in kernels.items()},
             },
             "clocks": clocks,
             "e2e": {"value": e2e_value, "unit": "TFLOPS", "h2d_bytes_per_step": h2d,

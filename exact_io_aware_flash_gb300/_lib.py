@@ -52,7 +52,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.fa_backward.restype = i
         lib.fa_backward_noalloc.argtypes = [vp] * 9 + [i] * 6 + [f, i, vp]
         lib.fa_backward_noalloc.restype = i
-        lib.fa_set_backward_event_hooks.argtypes = [vp, vp]
+        lib.fa_set_backward_event_hooks.argtypes = [vp, vp, vp]
         lib.fa_set_backward_event_hooks.restype = i
         lib.fa_check_errors.argtypes = [vp]
         lib.fa_check_errors.restype = i
@@ -159,15 +159,14 @@ def backward(q, k, v, o, lse, dO, causal: bool = False, scale: float | None = No
     return dq, dk, dv
 
 
-def set_backward_event_hooks(before=None, after=None) -> None:
-    """Record CUDA events around the backward's main kernel (see fa.h); None, None stops.
+def set_backward_event_hooks(before_dkdv=None, before_dq=None, after_dq=None) -> None:
+    """Record CUDA events around the backward's dK/dV and dQ kernels (see fa.h).
 
-    ``before`` / ``after`` are torch.cuda.Event objects that have been recorded
-    at least once (so their CUDA handles exist).
+    The arguments are torch.cuda.Event objects that have been recorded at
+    least once (so their CUDA handles exist); three Nones stop the hook.
     """
-    hb = None if before is None else before.cuda_event
-    ha = None if after is None else after.cuda_event
-    _raise(load().fa_set_backward_event_hooks(hb, ha))
+    evs = (before_dkdv, before_dq, after_dq)
+    _raise(load().fa_set_backward_event_hooks(*(None if e is None else e.cuda_event for e in evs)))
 
 
 def check_errors(stream=None) -> None:

@@ -18,8 +18,7 @@ namespace {
 __device__ int g_fa_error_word;
 
 thread_local std::string t_last_error;
-thread_local cudaEvent_t t_ev_before = nullptr;
-thread_local cudaEvent_t t_ev_after = nullptr;
+thread_local cudaEvent_t t_ev_hooks[3] = {nullptr, nullptr, nullptr};
 
 int fail(int code, const char* fmt, ...) {
   char buf[512];
@@ -119,11 +118,10 @@ int check_common(int B, int Hq, int Hkv, int N, int d, float scale, int dtype) {
   if (d != 64 && d != 128) return fail(FA_ERR_UNSUPPORTED, "head dimension d=%d (supported: 64, 128)", d);
   if (dtype != FA_DTYPE_FP16 && dtype != FA_DTYPE_BF16)
     return fail(FA_ERR_UNSUPPORTED, "dtype %d (supported: FA_DTYPE_FP16, FA_DTYPE_BF16)", dtype);
-  // grid.y carries pairs of 128-row query tiles; grid.x carries B*Hq.
-  const long long pairs = ((long long)N + 255) / 256;
-  if (pairs > 65535) return fail(FA_ERR_UNSUPPORTED, "N=%d exceeds the supported maximum", N);
-  if ((long long)B * Hq > 0x7fffffffLL || (long long)B * Hq * N > 0x7fffffffLL)
-    return fail(FA_ERR_UNSUPPORTED, "B*Hq*N exceeds 2^31-1");
+  // grid.y carries the (batch, head) index of the forward and backward grids.
+  if ((long long)B * Hq > 65535)
+    return fail(FA_ERR_UNSUPPORTED, "B*Hq=%lld exceeds 65535", (long long)B * Hq);
+  if ((long long)B * Hq * N > 0x7fffffffLL) return fail(FA_ERR_UNSUPPORTED, "B*Hq*N exceeds 2^31-1");
   return FA_OK;
 }
 
@@ -177,7 +175,7 @@ int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse,
 size_t fa_backward_workspace_size(int B, int Hq, int N, int d) {
   if (B <= 0 || Hq <= 0 || N <= 0 || d <= 0) return 0;
   const size_t rows = static_cast<size_t>(B) * Hq * N;
-  return round_up(rows * 4, 256) + rows * static_cast<size_t>(d) * 4;
+  return round_up(rows * 4, 256);
 }
 
 int fa_backward(const void* q, const void* k, const void* v, const void* o, const float* lse,
@@ -205,29 +203,29 @@ int fa_backward(const void* q, const void* k, const void* v, const void* o, cons
   if ((rc = encode_tile_map(&a.tm_k, k, B * Hkv, N, d, s.bf16, "k"))) return rc;
   if ((rc = encode_tile_map(&a.tm_v, v, B * Hkv, N, d, s.bf16, "v"))) return rc;
   if ((rc = encode_tile_map(&a.tm_do, dO, B * Hq, N, d, s.bf16, "dO"))) return rc;
-  const size_t rows = static_cast<size_t>(B) * Hq * N;
   a.o = o;
   a.dO = dO;
   a.lse = lse;
   a.D = static_cast<float*>(workspace);
-  a.dq_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + round_up(rows * 4, 256));
   a.dq = dq;
   a.dk = dk;
   a.dv = dv;
   a.err = st->err_word;
-  a.ev_before_main = t_ev_before;
-  a.ev_after_main = t_ev_after;
+  a.ev_before_dkdv = t_ev_hooks[0];
+  a.ev_before_dq = t_ev_hooks[1];
+  a.ev_after_dq = t_ev_hooks[2];
   cudaError_t e = fa::launch_backward(s, a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(FA_ERR_CUDA, "backward launch: %s", cudaGetErrorString(e));
   return FA_OK;
 }
 
-int fa_set_backward_event_hooks(void* before, void* after) {
+int fa_set_backward_event_hooks(void* before_dkdv, void* before_dq, void* after_dq) {
   t_last_error.clear();
-  if ((before == nullptr) != (after == nullptr))
-    return fail(FA_ERR_INVALID, "pass both events or neither");
-  t_ev_before = static_cast<cudaEvent_t>(before);
-  t_ev_after = static_cast<cudaEvent_t>(after);
+  const int n = (before_dkdv != nullptr) + (before_dq != nullptr) + (after_dq != nullptr);
+  if (n != 0 && n != 3) return fail(FA_ERR_INVALID, "pass all three events or none");
+  t_ev_hooks[0] = static_cast<cudaEvent_t>(before_dkdv);
+  t_ev_hooks[1] = static_cast<cudaEvent_t>(before_dq);
+  t_ev_hooks[2] = static_cast<cudaEvent_t>(after_dq);
   return FA_OK;
 }
 

@@ -13,33 +13,29 @@
 //     dQ   = scale * dS K,   dK = scale * dS^T Q
 //
 // Kernels, all on the caller's stream:
-//   fa_bwd_pre_kernel   D = rowsum(dO o O) and zero the fp32 dQ accumulator.
-//   fa_bwd_kernel       one CTA per (KV head, 128-key tile j); loops over the
-//                       KV head's query heads and query tiles i (causal: i >= j).
-//                       Transposed formulation, so that the key tile owns the
-//                       TMEM lanes and dK, dV accumulate in Tensor Memory over
-//                       the whole loop (no atomics for dK / dV, and GQA groups
-//                       are summed in-kernel):
-//                         S^T  = K_j Q_i^T          tcgen05, SMEM x SMEM
-//                         dP^T = V_j dO_i^T         tcgen05, SMEM x SMEM
-//                         P^T, dS^T                 compute warps (exp2, fp32)
-//                         dV  += P^T dO_i           tcgen05, P^T from TMEM
-//                         dK  += dS^T Q_i           tcgen05, dS^T from SMEM
-//                         dQ_i = dS K_j             tcgen05, dS^T read MN-major
-//                         dQacc_i += dQ_i           fp32 vector atomics
-//                       The primer notes that the default backward accumulates
-//                       dQ across thread blocks with atomic adds (section
-//                       "Backward pass: recomputation instead of storage"); so
-//                       does this one.
-//   fa_bwd_dq_kernel    dq = scale * dQacc, converted to the 16-bit type.
+//   fa_bwd_pre_kernel    D = rowsum(dO o O).
+//   fa_bwd_dkdv_kernel   one CTA per (KV head, 128-key tile j), looping over the
+//                        KV head's query heads and query tiles i (causal: i >= j),
+//                        in the transposed orientation so the key tile owns the
+//                        TMEM lanes and dK, dV accumulate in Tensor Memory:
+//                          S^T  = K_j Q_i^T,  dP^T = V_j dO_i^T   (SMEM x SMEM)
+//                          P^T, dS^T                           (compute warps)
+//                          dV  += P^T dO_i,   dK  += dS^T Q_i     (TMEM A operand)
+//   fa_bwd_dq_kernel     one CTA per (query head, 128-query tile i), looping over
+//                        key tiles j (causal: j <= i), dQ accumulating in TMEM:
+//                          S = Q_i K_j^T,  dP = dO_i V_j^T        (SMEM x SMEM)
+//                          P, dS                               (compute warps)
+//                          dQ += dS K_j                        (TMEM A operand)
+// dQ is therefore summed over key tiles inside one CTA rather than with atomic
+// adds across CTAs (the primer notes the default backward uses atomic adds and
+// is nondeterministic, section "Backward pass: recomputation instead of
+// storage").  Every gradient is summed in a fixed order, so the backward is
+// bitwise deterministic; the price is recomputing S and dP in both kernels
+// (7 instead of 5 N x N x d products).
 //
-// Warp roles of fa_bwd_kernel (10 warps):
-//   warps 0-3  compute: thread t owns key row t of the tile (TMEM lane t).
-//   warps 4-7  dQ readout + dK epilogue.
-//   warp 8     producer: K_j, V_j once; Q_i, dO_i through a 2-stage ring (TMA);
-//              LSE_i and D_i for the tile into shared memory (plain loads).
-//   warp 9     MMA issuer (one thread) and TMEM allocator.
-// TMEM columns: dV [0,128), dK [128,256), S^T / P^T [256,384), dP^T / dQ [384,512).
+// Both main kernels use 6 warps: warps 0-3 compute (thread t owns row t of the
+// tile, TMEM lane t), warp 4 is the TMA producer, warp 5 the single-thread MMA
+// issuer and TMEM allocator.
 #include "fa_internal.h"
 #include "ptx.cuh"
 
@@ -51,38 +47,8 @@ namespace {
 
 constexpr int kBlk = 128;          // rows per tile (keys and queries)
 constexpr int kAtomBytes = 16384;  // 128 rows x 128 bytes
-constexpr int kThreads = 320;
+constexpr int kThreads = 192;
 constexpr float kLog2e = 1.4426950408889634f;
-
-template <int D>
-struct BwdSmem {
-  static constexpr int kTile = kBlk * D * 2;
-  static constexpr int kK = 0;
-  static constexpr int kV = kK + kTile;
-  static constexpr int kQ = kV + kTile;        // 2 stages
-  static constexpr int kdO = kQ + 2 * kTile;   // 2 stages
-  static constexpr int kdS = kdO + 2 * kTile;  // dS^T, 128 x 128 16-bit = 32 KB
-  static constexpr int kLse = kdS + 32768;     // 128 floats: LSE * log2(e)
-  static constexpr int kDrow = kLse + 512;     // 128 floats: D
-  static constexpr int kBar = kDrow + 512;
-  static constexpr int kBytes = kBar + 256;
-  static constexpr int kAlloc = kBytes + 1024;
-};
-
-enum BwdBars {
-  BKV = 0,
-  BQFULL = 1,   // +stage
-  BQEMPTY = 3,  // +stage
-  BLDFULL = 5,
-  BLDEMPTY = 6,
-  BSDP = 7,     // S^T and dP^T in TMEM
-  BPDS = 8,     // P^T in TMEM and dS^T in SMEM
-  BDVDONE = 9,  // dV MMA of this iteration done (S/P columns free)
-  BDQ = 10,     // dQ tile in TMEM
-  BDQFREE = 11, // dQ tile read out (dP/dQ columns free)
-  BFINAL = 12,
-  NBWDBARS = 13
-};
 
 template <bool BF16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
@@ -113,64 +79,21 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
-// ------------------------------------------------------------------ preprocessing
-// D_i = sum_c dO_ic O_ic (fp32) and dQacc = 0.  D/8 threads per row, 16 bytes each.
-template <int D, bool BF16>
-__global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const uint4* __restrict__ O,
-                                                         const uint4* __restrict__ dO,
-                                                         float* __restrict__ Drow,
-                                                         float4* __restrict__ dq_acc, long rows) {
-  constexpr int kTpr = D / 8;  // threads per row
-  const long total = rows * kTpr;
-  const long stride = static_cast<long>(gridDim.x) * blockDim.x;
-  const int lane = threadIdx.x & 31;
-  const int sub = threadIdx.x % kTpr;
-  // Whole warps iterate together so the row reduction's shuffles see all lanes.
-  for (long w0 = static_cast<long>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31); w0 < total;
-       w0 += stride) {
-    const long t = w0 + lane;
-    const bool in = t < total;
-    const long row = t / kTpr;
-    float acc = 0.f;
-    if (in) {
-      const uint4 a = O[t];
-      const uint4 b = dO[t];
-      const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
-      const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 x = unpack2<BF16>(aw[e]);
-        const float2 y = unpack2<BF16>(bw[e]);
-        acc = fmaf(x.x, y.x, acc);
-        acc = fmaf(x.y, y.y, acc);
-      }
-    }
-#pragma unroll
-    for (int off = kTpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (in) {
-      if (sub == 0) Drow[row] = acc;
-      const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-      dq_acc[row * (D / 4) + 2 * sub] = z;
-      dq_acc[row * (D / 4) + 2 * sub + 1] = z;
-    }
-  }
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) &
+                                    ~static_cast<uintptr_t>(1023));
 }
 
-// dq = scale * dQacc in the 16-bit type; 8 elements per thread.
-template <bool BF16>
-__global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const float4* __restrict__ acc,
-                                                        uint4* __restrict__ dq, long n8,
-                                                        float scale) {
-  const long stride = static_cast<long>(gridDim.x) * blockDim.x;
-  for (long t = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x; t < n8; t += stride) {
-    const float4 a = acc[2 * t];
-    const float4 b = acc[2 * t + 1];
-    dq[t] = make_uint4(pack2<BF16>(a.x * scale, a.y * scale), pack2<BF16>(a.z * scale, a.w * scale),
-                       pack2<BF16>(b.x * scale, b.y * scale), pack2<BF16>(b.z * scale, b.w * scale));
-  }
+// K-major operand (rows of 128 bytes, 8-row groups 1024 bytes apart), k-step ks of 16 elements.
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile, int ks) {
+  return sdesc_sw128(tile + (ks >> 2) * kAtomBytes + (ks & 3) * 32, 16, 1024);
+}
+// MN-major operand over a [128 K-rows][D] tile, k-step ks of 16 K-rows.
+__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile, int ks) {
+  return sdesc_sw128(tile + ks * 2048, kAtomBytes, 1024);
 }
 
-// ------------------------------------------------------------------ main kernel
+// TMEM row (D fp32 columns at taddr) * mul -> 16-bit row in global memory.
 template <int D, bool BF16>
 __device__ __forceinline__ void store_rows_from_tmem(uint32_t taddr, uint16_t* row, float mul,
                                                      bool valid) {
@@ -193,28 +116,92 @@ __device__ __forceinline__ void store_rows_from_tmem(uint32_t taddr, uint16_t* r
   }
 }
 
+// ------------------------------------------------------------------ preprocessing
+// D_i = sum_c dO_ic O_ic (fp32).  D/8 threads per row, 16 bytes each.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const uint4* __restrict__ O,
+                                                         const uint4* __restrict__ dO,
+                                                         float* __restrict__ Drow, long rows) {
+  constexpr int kTpr = D / 8;  // threads per row
+  const long total = rows * kTpr;
+  const long stride = static_cast<long>(gridDim.x) * blockDim.x;
+  const int lane = threadIdx.x & 31;
+  const int sub = threadIdx.x % kTpr;
+  // Whole warps iterate together so the row reduction's shuffles see all lanes.
+  for (long w0 = static_cast<long>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31); w0 < total;
+       w0 += stride) {
+    const long t = w0 + lane;
+    const bool in = t < total;
+    float acc = 0.f;
+    if (in) {
+      const uint4 a = O[t];
+      const uint4 b = dO[t];
+      const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
+      const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 x = unpack2<BF16>(aw[e]);
+        const float2 y = unpack2<BF16>(bw[e]);
+        acc = fmaf(x.x, y.x, acc);
+        acc = fmaf(x.y, y.y, acc);
+      }
+    }
+#pragma unroll
+    for (int off = kTpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (in && sub == 0) Drow[t / kTpr] = acc;
+  }
+}
+
+// ------------------------------------------------------------------ dK, dV
+template <int D>
+struct DkdvSmem {
+  static constexpr int kTile = kBlk * D * 2;
+  static constexpr int kK = 0;
+  static constexpr int kV = kK + kTile;
+  static constexpr int kQ = kV + kTile;        // 2 stages
+  static constexpr int kdO = kQ + 2 * kTile;   // 2 stages
+  static constexpr int kLse = kdO + 2 * kTile; // 2 stages x 128 floats: LSE * log2(e)
+  static constexpr int kDrow = kLse + 1024;    // 2 stages x 128 floats: D
+  static constexpr int kBar = kDrow + 1024;
+  static constexpr int kBytes = kBar + 256;
+  static constexpr int kAlloc = kBytes + 1024;
+};
+
+enum DkdvBars {
+  KB_KV = 0,
+  KB_QFULL = 1,   // +stage: Q_i, dO_i (TMA) and LSE_i, D_i (32 producer lanes)
+  KB_QEMPTY = 3,  // +stage
+  KB_SFULL = 5,   // S^T in TMEM
+  KB_DPFULL = 6,  // dP^T in TMEM
+  KB_PREADY = 7,  // P^T written to TMEM (4 warps)
+  KB_DSREADY = 8, // dS^T written to TMEM (4 warps)
+  KB_DVDONE = 9,  // dV MMA done: S^T columns free
+  KB_DKDONE = 10, // dK MMA done: dP^T columns free
+  KB_FINAL = 11,
+  KB_N = 12
+};
+
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
-    fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                  const float* __restrict__ lse, const float* __restrict__ Drow,
-                  float* __restrict__ dq_acc, void* __restrict__ dk_out, void* __restrict__ dv_out,
-                  int Hq, int Hkv, int N, int causal, float scale, int* err) {
-  using L = BwdSmem<D>;
+    fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                       const float* __restrict__ lse, const float* __restrict__ Drow,
+                       void* __restrict__ dk_out, void* __restrict__ dv_out, int Hq, int Hkv, int N,
+                       int causal, float scale, int* err) {
+  using L = DkdvSmem<D>;
   constexpr int kAtoms = D / 64;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* smem = align1024(smem_raw);
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::kBar);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + NBWDBARS);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + KB_N);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float* s_lse = reinterpret_cast<float*>(smem + L::kLse);
-  float* s_d = reinterpret_cast<float*>(smem + L::kDrow);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int bkv = blockIdx.x;  // b * Hkv + hkv
-  const int j = blockIdx.y;    // key tile; small j has the most work under causal
+  // All key tiles of one KV head run side by side (that head's Q and dO stay
+  // in L2); within a head j = 0, the most work under causal masking, first.
+  const int j = blockIdx.x;
+  const int bkv = blockIdx.y;  // b * Hkv + hkv
   const int b = bkv / Hkv;
   const int hkv = bkv % Hkv;
   const int group = Hq / Hkv;
@@ -222,18 +209,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int i0 = causal ? j : 0;
   const int n_i = T - i0;
   const int n_it = group * n_i;
+  constexpr uint32_t kColDV = 0, kColDK = 128, kColS = 256, kColDP = 384;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < NBWDBARS; ++i) {
+    for (int i = 0; i < KB_N; ++i) {
       uint32_t cnt = 1;
-      if (i == BLDFULL) cnt = 32;
-      if (i == BLDEMPTY || i == BPDS || i == BDQFREE) cnt = 4;
+      if (i == KB_QFULL || i == KB_QFULL + 1) cnt = 33;
+      if (i == KB_PREADY || i == KB_DSREADY) cnt = 4;
       mbar_init(&bar[i], cnt);
     }
     *abort_flag = (*reinterpret_cast<volatile int*>(err) != kDevErrNone) ? 1 : 0;
     fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == 5) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
@@ -241,24 +229,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const bool run = (*abort_flag == 0);
-  constexpr uint32_t kColDV = 0, kColDK = 128, kColS = 256, kColDP = 384;
 
-  if (run && warp == 8) {
+  if (run && warp == 4) {
     // ------------------------------------------------------------ producer
-    const uint64_t pol_kv = l2_policy_evict_first();
-    const uint64_t pol_q = l2_policy_evict_last();
+    float* s_lse = reinterpret_cast<float*>(smem + L::kLse);
+    float* s_d = reinterpret_cast<float*>(smem + L::kDrow);
     int issued = 0;
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       tma_prefetch_desc(&tm_do);
-      mbar_expect_tx(&bar[BKV], 2 * L::kTile);
+      const uint64_t pol = l2_policy_evict_first();
+      mbar_expect_tx(&bar[KB_KV], 2 * L::kTile);
       for (int a = 0; a < kAtoms; ++a) {
-        tma_load_3d(smem + L::kK + a * kAtomBytes, &tm_k, &bar[BKV], a * 64, j * kBlk, bkv, pol_kv);
-        tma_load_3d(smem + L::kV + a * kAtomBytes, &tm_v, &bar[BKV], a * 64, j * kBlk, bkv, pol_kv);
+        tma_load_3d(smem + L::kK + a * kAtomBytes, &tm_k, &bar[KB_KV], a * 64, j * kBlk, bkv, pol);
+        tma_load_3d(smem + L::kV + a * kAtomBytes, &tm_v, &bar[KB_KV], a * 64, j * kBlk, bkv, pol);
       }
     }
+    const uint64_t pol_q = l2_policy_evict_last();
     for (int it = 0; it < n_it; ++it) {
       const int hq = hkv * group + it / n_i;
       const int i = i0 + it % n_i;
@@ -266,100 +255,102 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int st = it & 1;
       bool ok = true;
       if (lane == 0) {
-        ok = mbar_wait(&bar[BQEMPTY + st], ((it >> 1) & 1) ^ 1, abort_flag, err);
+        ok = mbar_wait(&bar[KB_QEMPTY + st], ((it >> 1) & 1) ^ 1, abort_flag, err);
         if (ok) {
-          mbar_expect_tx(&bar[BQFULL + st], 2 * L::kTile);
+          mbar_expect_tx(&bar[KB_QFULL + st], 2 * L::kTile);
           for (int a = 0; a < kAtoms; ++a) {
-            tma_load_3d(smem + L::kQ + st * L::kTile + a * kAtomBytes, &tm_q, &bar[BQFULL + st],
+            tma_load_3d(smem + L::kQ + st * L::kTile + a * kAtomBytes, &tm_q, &bar[KB_QFULL + st],
                         a * 64, i * kBlk, bhq, pol_q);
-            tma_load_3d(smem + L::kdO + st * L::kTile + a * kAtomBytes, &tm_do, &bar[BQFULL + st],
+            tma_load_3d(smem + L::kdO + st * L::kTile + a * kAtomBytes, &tm_do, &bar[KB_QFULL + st],
                         a * 64, i * kBlk, bhq, pol_q);
           }
           issued = it + 1;
         }
       }
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      if (ok && it > 0) ok = __all_sync(0xffffffffu, mbar_wait(&bar[BLDEMPTY], (it - 1) & 1, abort_flag, err));
-      if (!ok) break;
-      // LSE (as log2) and D of the 128 query rows of this tile; padding rows get
-      // LSE = +inf so that their recomputed probabilities are exactly 0.
+      if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) == 0) break;  // also orders the stage reuse
+      // LSE (as log2) and D of the tile's 128 query rows; padding rows get
+      // LSE = +inf so their recomputed probabilities are exactly 0.
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int r = lane * 4 + e;
         const int qrow = i * kBlk + r;
         const size_t g = static_cast<size_t>(bhq) * N + qrow;
         const bool in = qrow < N;
-        s_lse[r] = in ? lse[g] * kLog2e : INFINITY;
-        s_d[r] = in ? Drow[g] : 0.f;
+        s_lse[st * 128 + r] = in ? lse[g] * kLog2e : INFINITY;
+        s_d[st * 128 + r] = in ? Drow[g] : 0.f;
       }
-      mbar_arrive(&bar[BLDFULL]);
+      mbar_arrive(&bar[KB_QFULL + st]);
     }
     if (lane == 0 && *abort_flag) {
-      drain_wait(&bar[BKV], 0);
+      drain_wait(&bar[KB_KV], 0);
       for (int it = (issued > 2 ? issued - 2 : 0); it < issued; ++it)
-        drain_wait(&bar[BQFULL + (it & 1)], (it >> 1) & 1);
+        drain_wait(&bar[KB_QFULL + (it & 1)], (it >> 1) & 1);
     }
-  } else if (run && warp == 9) {
+  } else if (run && warp == 5) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_f16(kBlk, kBlk, BF16, false, false);  // S^T, dP^T
       constexpr uint32_t kIdKV = idesc_f16(kBlk, D, BF16, false, true);     // dV, dK
-      constexpr uint32_t kIdQ = idesc_f16(kBlk, D, BF16, true, true);       // dQ
       const uint32_t sk = smem_u32(smem + L::kK);
       const uint32_t sv = smem_u32(smem + L::kV);
       const uint32_t sq = smem_u32(smem + L::kQ);
       const uint32_t sdo = smem_u32(smem + L::kdO);
-      const uint32_t sds = smem_u32(smem + L::kdS);
-      bool ok = mbar_wait(&bar[BKV], 0, abort_flag, err);
+      auto issue_s = [&](int st) {  // S^T = K_j Q_i^T
+        const uint32_t qa = sq + st * L::kTile;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          mma_ss(tmem + kColS, kmajor_desc(sk, ks), kmajor_desc(qa, ks), kIdS, ks > 0);
+        mma_commit(&bar[KB_SFULL]);
+      };
+      auto issue_dp = [&](int st) {  // dP^T = V_j dO_i^T
+        const uint32_t doa = sdo + st * L::kTile;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          mma_ss(tmem + kColDP, kmajor_desc(sv, ks), kmajor_desc(doa, ks), kIdS, ks > 0);
+        mma_commit(&bar[KB_DPFULL]);
+      };
+      bool ok = mbar_wait(&bar[KB_KV], 0, abort_flag, err) &&
+                mbar_wait(&bar[KB_QFULL], 0, abort_flag, err);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+        issue_dp(0);
+      }
       for (int it = 0; ok && it < n_it; ++it) {
         const int st = it & 1;
-        if (!(ok = mbar_wait(&bar[BQFULL + st], (it >> 1) & 1, abort_flag, err))) break;
-        if (it > 0 && !(ok = mbar_wait(&bar[BDVDONE], (it - 1) & 1, abort_flag, err))) break;
-        tc_fence_after();
         const uint32_t qa = sq + st * L::kTile;
         const uint32_t doa = sdo + st * L::kTile;
-        // S^T = K_j Q_i^T
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * kAtomBytes + (ks & 3) * 32;
-          mma_ss(tmem + kColS, sdesc_sw128(sk + off, 16, 1024), sdesc_sw128(qa + off, 16, 1024),
-                 kIdS, ks > 0);
-        }
-        if (it > 0 && !(ok = mbar_wait(&bar[BDQFREE], (it - 1) & 1, abort_flag, err))) break;
+        // dV += P^T dO_i   (P^T: 16-bit pairs over the first half of the S^T columns)
+        if (!(ok = mbar_wait(&bar[KB_PREADY], it & 1, abort_flag, err))) break;
         tc_fence_after();
-        // dP^T = V_j dO_i^T
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * kAtomBytes + (ks & 3) * 32;
-          mma_ss(tmem + kColDP, sdesc_sw128(sv + off, 16, 1024), sdesc_sw128(doa + off, 16, 1024),
-                 kIdS, ks > 0);
-        }
-        mma_commit(&bar[BSDP]);
-        if (!(ok = mbar_wait(&bar[BPDS], it & 1, abort_flag, err))) break;
-        tc_fence_after();
-        // dV += P^T dO_i   (P^T: 16-bit pairs in TMEM over the first half of S^T)
 #pragma unroll
         for (int ks = 0; ks < kBlk / 16; ++ks)
-          mma_ts(tmem + kColDV, tmem + kColS + ks * 8, sdesc_sw128(doa + ks * 2048, kAtomBytes, 1024),
-                 kIdKV, (it > 0 || ks > 0) ? 1u : 0u);
-        mma_commit(&bar[BDVDONE]);
-        // dK += dS^T Q_i   (dS^T in SMEM, K-major over the query index)
-#pragma unroll
-        for (int ks = 0; ks < kBlk / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * kAtomBytes + (ks & 3) * 32;
-          mma_ss(tmem + kColDK, sdesc_sw128(sds + off, 16, 1024),
-                 sdesc_sw128(qa + ks * 2048, kAtomBytes, 1024), kIdKV, (it > 0 || ks > 0) ? 1u : 0u);
-        }
-        // dQ_i = dS K_j   (the same dS^T buffer read MN-major; K_j as an MN-major B)
+          mma_ts(tmem + kColDV, tmem + kColS + ks * 8, mnmajor_desc(doa, ks), kIdKV,
+                 (it > 0 || ks > 0) ? 1u : 0u);
+        mma_commit(&bar[KB_DVDONE]);
+        // dK += dS^T Q_i   (dS^T: 16-bit pairs over the first half of the dP^T columns)
+        if (!(ok = mbar_wait(&bar[KB_DSREADY], it & 1, abort_flag, err))) break;
+        tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < kBlk / 16; ++ks)
-          mma_ss(tmem + kColDP, sdesc_sw128(sds + ks * 2048, kAtomBytes, 1024),
-                 sdesc_sw128(sk + ks * 2048, kAtomBytes, 1024), kIdQ, ks > 0);
-        mma_commit(&bar[BDQ]);
-        mma_commit(&bar[BQEMPTY + st]);
+          mma_ts(tmem + kColDK, tmem + kColDP + ks * 8, mnmajor_desc(qa, ks), kIdKV,
+                 (it > 0 || ks > 0) ? 1u : 0u);
+        mma_commit(&bar[KB_DKDONE]);
+        mma_commit(&bar[KB_QEMPTY + st]);
+        if (it + 1 < n_it) {
+          const int st1 = (it + 1) & 1;
+          if (!(ok = mbar_wait(&bar[KB_QFULL + st1], ((it + 1) >> 1) & 1, abort_flag, err))) break;
+          // S^T(it+1) overwrites the columns dV(it) reads; dP^T(it+1) those dK(it) reads.
+          if (!(ok = mbar_wait(&bar[KB_DVDONE], it & 1, abort_flag, err))) break;
+          tc_fence_after();
+          issue_s(st1);
+          if (!(ok = mbar_wait(&bar[KB_DKDONE], it & 1, abort_flag, err))) break;
+          tc_fence_after();
+          issue_dp(st1);
+        }
       }
-      mma_commit(&bar[BFINAL]);
-      drain_wait(&bar[BFINAL], 0);
+      mma_commit(&bar[KB_FINAL]);
+      drain_wait(&bar[KB_FINAL], 0);
     }
   } else if (run && warp < 4) {
     // ------------------------------------------------------------ compute: P^T, dS^T
@@ -368,115 +359,354 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tmem + lane_off + kColS;
     const uint32_t tP = tmem + lane_off + kColDP;
     const float sl2 = scale * kLog2e;
-    uint8_t* sds = smem + L::kdS;
+    const float* s_lse = reinterpret_cast<const float*>(smem + L::kLse);
+    const float* s_d = reinterpret_cast<const float*>(smem + L::kDrow);
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
       const int i = i0 + it % n_i;
-      ok = __all_sync(0xffffffffu, mbar_wait(&bar[BSDP], it & 1, abort_flag, err) &&
-                                       mbar_wait(&bar[BLDFULL], it & 1, abort_flag, err));
+      const int st = it & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(&bar[KB_SFULL], it & 1, abort_flag, err) &&
+                                       mbar_wait(&bar[KB_QFULL + st], (it >> 1) & 1, abort_flag, err));
       if (!ok) break;
       tc_fence_after();
       const bool diag = causal && (i == j);
+      const float* lse2 = s_lse + st * 128;
+      const float* dd = s_d + st * 128;
+      // P^T row t: exp2(s * scale*log2(e) - LSE_q*log2(e)); query q before key t is masked.
+      float p[kBlk];
+#pragma unroll
+      for (int h = 0; h < kBlk; h += 64) {  // two halves keep the live registers below the cap
+        uint32_t sv[64];
+        tmem_ld32(tS + h, sv);
+        tmem_ld32(tS + h + 32, sv + 32);
+        tmem_ld_wait();
+        reg_fence<64>(sv);
+#pragma unroll
+        for (int c = 0; c < 64; c += 4) {
+          const float4 l4 = lds128_ordered(lse2 + h + c);
+          p[h + c] = ex2_approx(fmaf(__uint_as_float(sv[c]), sl2, -l4.x));
+          p[h + c + 1] = ex2_approx(fmaf(__uint_as_float(sv[c + 1]), sl2, -l4.y));
+          p[h + c + 2] = ex2_approx(fmaf(__uint_as_float(sv[c + 2]), sl2, -l4.z));
+          p[h + c + 3] = ex2_approx(fmaf(__uint_as_float(sv[c + 3]), sl2, -l4.w));
+        }
+      }
+      if (diag) {
+#pragma unroll
+        for (int c = 0; c < kBlk; ++c)
+          if (c < t) p[c] = 0.f;
+      }
 #pragma unroll
       for (int c = 0; c < kBlk; c += 32) {
-        uint32_t sv[32], dpv[32];
-        tmem_ld32(tS + c, sv);
-        tmem_ld32(tP + c, dpv);
-        tmem_ld_wait();
-        reg_fence<32>(sv);
-        reg_fence<32>(dpv);
-        uint32_t pk[16], dk[16];
+        uint32_t pk[16];
 #pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          const float4 l4 = *reinterpret_cast<const float4*>(s_lse + c + e);
-          const float4 d4 = *reinterpret_cast<const float4*>(s_d + c + e);
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-          const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
-          float p[4], ds[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            float pv = ex2_approx(fmaf(__uint_as_float(sv[e + u]), sl2, -lv[u]));
-            if (diag && (c + e + u) < t) pv = 0.f;  // query i*128+c+e+u before key j*128+t
-            p[u] = pv;
-            ds[u] = pv * (__uint_as_float(dpv[e + u]) - dv4[u]);
-          }
-          pk[e / 2] = pack2<BF16>(p[0], p[1]);
-          pk[e / 2 + 1] = pack2<BF16>(p[2], p[3]);
-          dk[e / 2] = pack2<BF16>(ds[0], ds[1]);
-          dk[e / 2 + 1] = pack2<BF16>(ds[2], ds[3]);
-        }
-        // P^T chunk over S^T columns already read (chunk c/32 -> columns c/2 .. c/2+15)
+        for (int e = 0; e < 16; ++e) pk[e] = pack2<BF16>(p[c + 2 * e], p[c + 2 * e + 1]);
         tmem_st16(tS + c / 2, pk);
-        // dS^T row t, query columns c..c+31: 64 bytes = four 16-byte chunks
-        const int atom = c >> 6;
-        const int ch0 = (c & 63) >> 3;
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          *reinterpret_cast<uint4*>(sds + atom * kAtomBytes + sw128_offset(t, ch0 + u)) =
-              make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
       }
       tmem_st_wait();
-      fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&bar[BLDEMPTY]);
-        mbar_arrive(&bar[BPDS]);
-      }
-    }
-    // dV epilogue
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bar[BFINAL], 0, abort_flag, err));
-    if (ok) {
-      tc_fence_after();
-      const int kv = j * kBlk + t;
-      uint16_t* row = reinterpret_cast<uint16_t*>(dv_out) + (static_cast<size_t>(bkv) * N + kv) * D;
-      store_rows_from_tmem<D, BF16>(tmem + lane_off + kColDV, row, 1.0f, kv < N);
-    }
-  } else if (run && warp < 8) {
-    // ------------------------------------------------------------ dQ readout, dK epilogue
-    const int t = threadIdx.x - 128;  // query row within the tile (TMEM lane)
-    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t tQ = tmem + lane_off + kColDP;
-    bool ok = true;
-    for (int it = 0; it < n_it; ++it) {
-      const int hq = hkv * group + it / n_i;
-      const int i = i0 + it % n_i;
-      ok = __all_sync(0xffffffffu, mbar_wait(&bar[BDQ], it & 1, abort_flag, err));
+      if (lane == 0) mbar_arrive(&bar[KB_PREADY]);
+      // dS^T = P^T o (dP^T - D_q), chunk by chunk; chunk c's 16-bit pairs land
+      // on dP^T columns already read.
+      ok = __all_sync(0xffffffffu, mbar_wait(&bar[KB_DPFULL], it & 1, abort_flag, err));
       if (!ok) break;
       tc_fence_after();
-      const int qrow = i * kBlk + t;
-      float4* dst = reinterpret_cast<float4*>(
-          dq_acc + (static_cast<size_t>(b * Hq + hq) * N + qrow) * D);
 #pragma unroll
-      for (int c = 0; c < D; c += 32) {
-        uint32_t v[32];
-        tmem_ld32(tQ + c, v);
+      for (int c = 0; c < kBlk; c += 32) {
+        uint32_t dpv[32];
+        tmem_ld32(tP + c, dpv);
         tmem_ld_wait();
-        reg_fence<32>(v);
-        if (qrow < N) {
+        reg_fence<32>(dpv);
+        uint32_t pk[16];
 #pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4)
-            atomicAdd(dst + c / 4 + q4,
-                      make_float4(__uint_as_float(v[4 * q4]), __uint_as_float(v[4 * q4 + 1]),
-                                  __uint_as_float(v[4 * q4 + 2]), __uint_as_float(v[4 * q4 + 3])));
+        for (int e = 0; e < 32; e += 4) {
+          const float4 d4 = lds128_ordered(dd + c + e);
+          pk[e / 2] = pack2<BF16>(p[c + e] * (__uint_as_float(dpv[e]) - d4.x),
+                                  p[c + e + 1] * (__uint_as_float(dpv[e + 1]) - d4.y));
+          pk[e / 2 + 1] = pack2<BF16>(p[c + e + 2] * (__uint_as_float(dpv[e + 2]) - d4.z),
+                                      p[c + e + 3] * (__uint_as_float(dpv[e + 3]) - d4.w));
         }
+        tmem_st16(tP + c / 2, pk);
       }
+      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bar[BDQFREE]);
+      if (lane == 0) mbar_arrive(&bar[KB_DSREADY]);
     }
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bar[BFINAL], 0, abort_flag, err));
+    // dV and dK epilogue
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bar[KB_FINAL], 0, abort_flag, err));
     if (ok) {
       tc_fence_after();
       const int kv = j * kBlk + t;
-      uint16_t* row = reinterpret_cast<uint16_t*>(dk_out) + (static_cast<size_t>(bkv) * N + kv) * D;
-      store_rows_from_tmem<D, BF16>(tmem + lane_off + kColDK, row, scale, kv < N);
+      const size_t off = (static_cast<size_t>(bkv) * N + kv) * D;
+      store_rows_from_tmem<D, BF16>(tmem + lane_off + kColDV, reinterpret_cast<uint16_t*>(dv_out) + off,
+                                    1.0f, kv < N);
+      store_rows_from_tmem<D, BF16>(tmem + lane_off + kColDK, reinterpret_cast<uint16_t*>(dk_out) + off,
+                                    scale, kv < N);
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == 5) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ------------------------------------------------------------------ dQ
+template <int D>
+struct DqSmem {
+  static constexpr int kTile = kBlk * D * 2;
+  static constexpr int kQ = 0;
+  static constexpr int kdO = kQ + kTile;
+  static constexpr int kK = kdO + kTile;       // 2 stages
+  static constexpr int kV = kK + 2 * kTile;    // 2 stages
+  static constexpr int kBar = kV + 2 * kTile;
+  static constexpr int kBytes = kBar + 256;
+  static constexpr int kAlloc = kBytes + 1024;
+};
+
+enum DqBars {
+  QB_Q = 0,       // Q_i, dO_i
+  QB_KFULL = 1,   // +stage
+  QB_KEMPTY = 3,  // +stage
+  QB_VFULL = 5,   // +stage
+  QB_VEMPTY = 7,  // +stage
+  QB_SFULL = 9,
+  QB_DPFULL = 10,
+  QB_SFREE = 11,   // S read into registers (4 warps)
+  QB_DPFREE = 12,  // dP read (4 warps)
+  QB_DSREADY = 13, // dS written to TMEM (4 warps)
+  QB_DQDONE = 14,  // dQ MMA done: dS columns free
+  QB_FINAL = 15,
+  QB_N = 16
+};
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                     const float* __restrict__ lse, const float* __restrict__ Drow,
+                     void* __restrict__ dq_out, int Hq, int Hkv, int N, int causal, float scale,
+                     int* err) {
+  using L = DqSmem<D>;
+  constexpr int kAtoms = D / 64;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::kBar);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + QB_N);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int T = (N + kBlk - 1) / kBlk;
+  // Query tiles of one head side by side (its K, V stay in L2); the tile with
+  // the most key tiles under causal masking first.
+  const int i = T - 1 - static_cast<int>(blockIdx.x);
+  const int bhq = blockIdx.y;  // b * Hq + hq
+  const int b = bhq / Hq;
+  const int hq = bhq % Hq;
+  const int kvh = b * Hkv + hq / (Hq / Hkv);
+  const int n_j = causal ? i + 1 : T;
+  constexpr uint32_t kColDQ = 0, kColS = 128, kColDP = 256, kColDS = 384;
+
+  if (threadIdx.x == 0) {
+    for (int k = 0; k < QB_N; ++k) {
+      uint32_t cnt = 1;
+      if (k == QB_SFREE || k == QB_DPFREE || k == QB_DSREADY) cnt = 4;
+      mbar_init(&bar[k], cnt);
+    }
+    *abort_flag = (*reinterpret_cast<volatile int*>(err) != kDevErrNone) ? 1 : 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const bool run = (*abort_flag == 0);
+
+  if (run && warp == 4) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_do);
+      const uint64_t pol_q = l2_policy_evict_first();
+      const uint64_t pol_kv = l2_policy_evict_last();
+      mbar_expect_tx(&bar[QB_Q], 2 * L::kTile);
+      for (int a = 0; a < kAtoms; ++a) {
+        tma_load_3d(smem + L::kQ + a * kAtomBytes, &tm_q, &bar[QB_Q], a * 64, i * kBlk, bhq, pol_q);
+        tma_load_3d(smem + L::kdO + a * kAtomBytes, &tm_do, &bar[QB_Q], a * 64, i * kBlk, bhq, pol_q);
+      }
+      int issued = 0;
+      for (int jj = 0; jj < n_j; ++jj) {
+        const int st = jj & 1;
+        const uint32_t ph = (jj >> 1) & 1;
+        if (!mbar_wait(&bar[QB_KEMPTY + st], ph ^ 1, abort_flag, err)) break;
+        mbar_expect_tx(&bar[QB_KFULL + st], L::kTile);
+        for (int a = 0; a < kAtoms; ++a)
+          tma_load_3d(smem + L::kK + st * L::kTile + a * kAtomBytes, &tm_k, &bar[QB_KFULL + st],
+                      a * 64, jj * kBlk, kvh, pol_kv);
+        if (!mbar_wait(&bar[QB_VEMPTY + st], ph ^ 1, abort_flag, err)) {
+          issued = 2 * jj + 1;
+          break;
+        }
+        mbar_expect_tx(&bar[QB_VFULL + st], L::kTile);
+        for (int a = 0; a < kAtoms; ++a)
+          tma_load_3d(smem + L::kV + st * L::kTile + a * kAtomBytes, &tm_v, &bar[QB_VFULL + st],
+                      a * 64, jj * kBlk, kvh, pol_kv);
+        issued = 2 * jj + 2;
+      }
+      if (*abort_flag) {
+        drain_wait(&bar[QB_Q], 0);
+        for (int x = (issued > 4 ? issued - 4 : 0); x < issued; ++x) {
+          const int jj = x >> 1, st = jj & 1;
+          drain_wait(&bar[((x & 1) ? QB_VFULL : QB_KFULL) + st], (jj >> 1) & 1);
+        }
+      }
+    }
+  } else if (run && warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdS = idesc_f16(kBlk, kBlk, BF16, false, false);  // S, dP
+      constexpr uint32_t kIdQ = idesc_f16(kBlk, D, BF16, false, true);      // dQ
+      const uint32_t sq = smem_u32(smem + L::kQ);
+      const uint32_t sdo = smem_u32(smem + L::kdO);
+      const uint32_t sk = smem_u32(smem + L::kK);
+      const uint32_t sv = smem_u32(smem + L::kV);
+      auto issue_s = [&](int st) {  // S = Q_i K_j^T
+        const uint32_t ka = sk + st * L::kTile;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          mma_ss(tmem + kColS, kmajor_desc(sq, ks), kmajor_desc(ka, ks), kIdS, ks > 0);
+        mma_commit(&bar[QB_SFULL]);
+      };
+      auto issue_dp = [&](int st) {  // dP = dO_i V_j^T; V_j is free again once this completes
+        const uint32_t va = sv + st * L::kTile;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          mma_ss(tmem + kColDP, kmajor_desc(sdo, ks), kmajor_desc(va, ks), kIdS, ks > 0);
+        mma_commit(&bar[QB_DPFULL]);
+        mma_commit(&bar[QB_VEMPTY + st]);
+      };
+      bool ok = mbar_wait(&bar[QB_Q], 0, abort_flag, err) &&
+                mbar_wait(&bar[QB_KFULL], 0, abort_flag, err);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+        ok = mbar_wait(&bar[QB_VFULL], 0, abort_flag, err);
+        if (ok) {
+          tc_fence_after();
+          issue_dp(0);
+        }
+      }
+      for (int jj = 0; ok && jj < n_j; ++jj) {
+        const int st = jj & 1;
+        if (jj + 1 < n_j) {
+          const int st1 = (jj + 1) & 1;
+          const uint32_t ph1 = ((jj + 1) >> 1) & 1;
+          // S(j+1) may start once S(j) has been read out of TMEM; dP(j+1) once dP(j) has.
+          if (!(ok = mbar_wait(&bar[QB_KFULL + st1], ph1, abort_flag, err))) break;
+          if (!(ok = mbar_wait(&bar[QB_SFREE], jj & 1, abort_flag, err))) break;
+          tc_fence_after();
+          issue_s(st1);
+          if (!(ok = mbar_wait(&bar[QB_VFULL + st1], ph1, abort_flag, err))) break;
+          if (!(ok = mbar_wait(&bar[QB_DPFREE], jj & 1, abort_flag, err))) break;
+          tc_fence_after();
+          issue_dp(st1);
+        }
+        // dQ += dS K_j   (dS: 16-bit pairs in its own TMEM columns; K_j as an MN-major B)
+        if (!(ok = mbar_wait(&bar[QB_DSREADY], jj & 1, abort_flag, err))) break;
+        tc_fence_after();
+        const uint32_t ka = sk + st * L::kTile;
+#pragma unroll
+        for (int ks = 0; ks < kBlk / 16; ++ks)
+          mma_ts(tmem + kColDQ, tmem + kColDS + ks * 8, mnmajor_desc(ka, ks), kIdQ,
+                 (jj > 0 || ks > 0) ? 1u : 0u);
+        mma_commit(&bar[QB_DQDONE]);
+        mma_commit(&bar[QB_KEMPTY + st]);
+      }
+      mma_commit(&bar[QB_FINAL]);
+      drain_wait(&bar[QB_FINAL], 0);
+    }
+  } else if (run && warp < 4) {
+    // ------------------------------------------------------------ compute: P, dS
+    const int t = threadIdx.x;  // query row within the tile
+    const int q = i * kBlk + t;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t tS = tmem + lane_off + kColS;
+    const uint32_t tP = tmem + lane_off + kColDP;
+    const uint32_t tDS = tmem + lane_off + kColDS;
+    const float sl2 = scale * kLog2e;
+    const size_t g = static_cast<size_t>(bhq) * N + q;
+    // Padding rows (q >= N) get LSE = +inf: P and dS are exactly 0 there.
+    const float lse2 = (q < N) ? lse[g] * kLog2e : INFINITY;
+    const float dq_d = (q < N) ? Drow[g] : 0.f;
+    bool ok = true;
+    for (int jj = 0; jj < n_j; ++jj) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&bar[QB_SFULL], jj & 1, abort_flag, err));
+      if (!ok) break;
+      tc_fence_after();
+      float p[kBlk];
+      {
+        uint32_t sv[kBlk];
+#pragma unroll
+        for (int c = 0; c < kBlk; c += 32) tmem_ld32(tS + c, sv + c);
+        tmem_ld_wait();
+        reg_fence<kBlk>(sv);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar[QB_SFREE]);
+#pragma unroll
+        for (int c = 0; c < kBlk; ++c) p[c] = ex2_approx(fmaf(__uint_as_float(sv[c]), sl2, -lse2));
+      }
+      if (causal && jj == i) {  // key j*128 + c after query i*128 + t is masked
+#pragma unroll
+        for (int c = 0; c < kBlk; ++c)
+          if (c > t) p[c] = 0.f;
+      }
+      ok = __all_sync(0xffffffffu, mbar_wait(&bar[QB_DPFULL], jj & 1, abort_flag, err));
+      // dS(j) overwrites the columns dQ(j-1) reads.
+      if (ok && jj > 0)
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar[QB_DQDONE], (jj - 1) & 1, abort_flag, err));
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < kBlk; c += 32) {
+        uint32_t dpv[32];
+        tmem_ld32(tP + c, dpv);
+        tmem_ld_wait();
+        reg_fence<32>(dpv);
+        uint32_t dsw[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          dsw[e] = pack2<BF16>(p[c + 2 * e] * (__uint_as_float(dpv[2 * e]) - dq_d),
+                               p[c + 2 * e + 1] * (__uint_as_float(dpv[2 * e + 1]) - dq_d));
+        tmem_st16(tDS + c / 2, dsw);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar[QB_DPFREE]);
+      if (lane == 0) mbar_arrive(&bar[QB_DSREADY]);
+    }
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bar[QB_FINAL], 0, abort_flag, err));
+    if (ok) {
+      tc_fence_after();
+      store_rows_from_tmem<D, BF16>(tmem + lane_off + kColDQ,
+                                    reinterpret_cast<uint16_t*>(dq_out) + g * D, scale, q < N);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -494,34 +724,40 @@ template <int D, bool BF16>
 cudaError_t launch_bwd_t(const AttnShape& s, const BwdArgs& a, cudaStream_t stream) {
   const long rows = static_cast<long>(s.B) * s.Hq * s.N;
   fa_bwd_pre_kernel<D, BF16><<<grid_for(rows * (D / 8), 256), 256, 0, stream>>>(
-      static_cast<const uint4*>(a.o), static_cast<const uint4*>(a.dO), a.D,
-      reinterpret_cast<float4*>(a.dq_acc), rows);
+      static_cast<const uint4*>(a.o), static_cast<const uint4*>(a.dO), a.D, rows);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
-  auto kern = fa_bwd_kernel<D, BF16>;
-  constexpr int smem = BwdSmem<D>::kAlloc;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
   const int T = (s.N + kBlk - 1) / kBlk;
-  dim3 grid(static_cast<unsigned>(s.B * s.Hkv), static_cast<unsigned>(T));
-  if (a.ev_before_main && (e = cudaEventRecord(a.ev_before_main, stream)) != cudaSuccess) return e;
-  kern<<<grid, kThreads, smem, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.lse, a.D, a.dq_acc,
-                                         a.dk, a.dv, s.Hq, s.Hkv, s.N, s.causal, s.scale, a.err);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  if (a.ev_after_main && (e = cudaEventRecord(a.ev_after_main, stream)) != cudaSuccess) return e;
+  auto kdkdv = fa_bwd_dkdv_kernel<D, BF16>;
+  constexpr int smem_kv = DkdvSmem<D>::kAlloc;
+  if ((e = cudaFuncSetAttribute(kdkdv, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_kv)) !=
+      cudaSuccess)
+    return e;
+  auto kdq = fa_bwd_dq_kernel<D, BF16>;
+  constexpr int smem_q = DqSmem<D>::kAlloc;
+  if ((e = cudaFuncSetAttribute(kdq, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_q)) !=
+      cudaSuccess)
+    return e;
 
-  const long n8 = rows * D / 8;
-  fa_bwd_dq_kernel<BF16><<<grid_for(n8, 256), 256, 0, stream>>>(
-      reinterpret_cast<const float4*>(a.dq_acc), static_cast<uint4*>(a.dq), n8, s.scale);
-  return cudaGetLastError();
+  if (a.ev_before_dkdv && (e = cudaEventRecord(a.ev_before_dkdv, stream)) != cudaSuccess) return e;
+  kdkdv<<<dim3(static_cast<unsigned>(T), static_cast<unsigned>(s.B * s.Hkv)), kThreads, smem_kv,
+          stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.lse, a.D, a.dk, a.dv, s.Hq, s.Hkv, s.N,
+                    s.causal, s.scale, a.err);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (a.ev_before_dq && (e = cudaEventRecord(a.ev_before_dq, stream)) != cudaSuccess) return e;
+  kdq<<<dim3(static_cast<unsigned>(T), static_cast<unsigned>(s.B * s.Hq)), kThreads, smem_q,
+        stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.lse, a.D, a.dq, s.Hq, s.Hkv, s.N, s.causal,
+                  s.scale, a.err);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (a.ev_after_dq && (e = cudaEventRecord(a.ev_after_dq, stream)) != cudaSuccess) return e;
+  return cudaSuccess;
 }
 
 }  // namespace
 
 size_t backward_smem_bytes(int d) {
-  return d == 64 ? BwdSmem<64>::kAlloc : BwdSmem<128>::kAlloc;
+  return d == 64 ? DkdvSmem<64>::kAlloc : DkdvSmem<128>::kAlloc;
 }
 
 cudaError_t launch_backward(const AttnShape& s, const BwdArgs& a, cudaStream_t stream) {

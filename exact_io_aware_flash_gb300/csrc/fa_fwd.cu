@@ -106,8 +106,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int bh = blockIdx.x;  // b * Hq + h
-  const int pair = gridDim.y - 1 - blockIdx.y;  // heaviest causal pairs first
+  // The query-tile pairs of one head run side by side so that head's K and V
+  // stay in L2; within a head the heaviest causal pairs are launched first.
+  const int pair = gridDim.x - 1 - blockIdx.x;
+  const int bh = blockIdx.y;  // b * Hq + h
   const int h = bh % Hq;
   const int b = bh / Hq;
   const int kvh = b * Hkv + h / (Hq / Hkv);
@@ -264,6 +266,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tO = tmem + lane_off + 256 + X * 128;
     float m_run = -INFINITY;
     float l_run = 0.f;
+    const bool pos_scale = scale_log2 > 0.f;
+    const float sfac = pos_scale ? scale_log2 : 1.0f;
     bool ok = true;
     for (int j = 0; j < nX; ++j) {
       ok = __all_sync(0xffffffffu, mbar_wait(&bar[BSFULL + X], j & 1, abort_flag, err));
@@ -277,18 +281,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       reg_fence<kBN>(x);
       const int kbase = j * kBN;
       const bool diag = causal && (j == t);
-      int lim = kBN;
-      if (diag || kbase + kBN > N) {
-        lim = N - kbase;
-        if (diag && r + 1 < lim) lim = r + 1;  // key kbase + c visible iff c <= r
-      }
-      float mx = -INFINITY;
+      // Scores stay raw when scale > 0 (the exponent is then one FFMA,
+      // s * scale*log2(e) - m, and the row maximum of raw scores times the
+      // positive factor is the maximum of the scaled scores); for scale <= 0
+      // they are scaled first and the factor below is 1.
+      if (!pos_scale) {
 #pragma unroll
-      for (int c = 0; c < kBN; ++c) {
-        const float v = (c < lim) ? __uint_as_float(x[c]) * scale_log2 : -INFINITY;
-        x[c] = __float_as_uint(v);
-        mx = fmaxf(mx, v);
+        for (int c = 0; c < kBN; ++c) x[c] = __float_as_uint(__uint_as_float(x[c]) * scale_log2);
       }
+      if (diag || kbase + kBN > N) {
+        int lim = N - kbase;
+        if (diag && r + 1 < lim) lim = r + 1;  // key kbase + c visible iff c <= r
+#pragma unroll
+        for (int c = 0; c < kBN; ++c)
+          if (c >= lim) x[c] = __float_as_uint(-INFINITY);
+      }
+      // row maximum as eight independent chains, then a tree
+      float m8[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) m8[u] = __uint_as_float(x[u]);
+#pragma unroll
+      for (int c = 8; c < kBN; ++c) m8[c & 7] = fmaxf(m8[c & 7], __uint_as_float(x[c]));
+      const float mx =
+          fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) *
+          sfac;
       // Conditional rescale: keep the stale maximum unless it grew by more than 8
       // (p <= 2^8 then); the decision is warp-uniform because TMEM access is.
       float alpha = 1.0f;
@@ -303,20 +319,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_run = mx;
         }
       }
-      float rowsum = 0.f;
+      float rs[4] = {0.f, 0.f, 0.f, 0.f};
+      const float neg_m = -m_run;
 #pragma unroll
       for (int c = 0; c < kBN; c += 32) {
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float p0 = ex2_approx(__uint_as_float(x[c + 2 * e]) - m_run);
-          const float p1 = ex2_approx(__uint_as_float(x[c + 2 * e + 1]) - m_run);
-          rowsum += p0 + p1;
+          const float p0 = ex2_approx(fmaf(__uint_as_float(x[c + 2 * e]), sfac, neg_m));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(x[c + 2 * e + 1]), sfac, neg_m));
+          rs[e & 3] += p0 + p1;
           pk[e] = pack2<BF16>(p0, p1);
         }
         tmem_st16(tS + c / 2, pk);
       }
-      l_run = l_run * alpha + rowsum;
+      l_run = l_run * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
       if (rescale) {
         // O_X was last written by PV_X(j-1), which completed before S_X(j) was issued.
 #pragma unroll
@@ -381,7 +398,7 @@ cudaError_t launch_fwd_t(const AttnShape& s, const FwdArgs& a, cudaStream_t stre
   if (e != cudaSuccess) return e;
   const int T = (s.N + kBM - 1) / kBM;
   const int pairs = (T + 1) / 2;
-  dim3 grid(static_cast<unsigned>(s.B * s.Hq), static_cast<unsigned>(pairs));
+  dim3 grid(static_cast<unsigned>(pairs), static_cast<unsigned>(s.B * s.Hq));
   const float scale_log2 = s.scale * 1.4426950408889634f;
   kern<<<grid, kThreads, smem, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.o, a.lse, s.Hq, s.Hkv, s.N,
                                          s.causal, scale_log2, a.err);

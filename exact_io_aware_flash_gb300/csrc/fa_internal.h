@@ -29,14 +29,16 @@ struct BwdArgs {
   const void* o;
   const void* dO;
   const float* lse;
-  float* D;       // [B*Hq*N]
-  float* dq_acc;  // [B*Hq*N*d]
+  float* D;  // [B*Hq*N]
   void* dq;
   void* dk;
   void* dv;
   int* err;
-  cudaEvent_t ev_before_main;  // may be null: recorded around the main kernel
-  cudaEvent_t ev_after_main;
+  // may be null: recorded before the dK/dV kernel, between it and the dQ
+  // kernel, and after the dQ kernel
+  cudaEvent_t ev_before_dkdv;
+  cudaEvent_t ev_before_dq;
+  cudaEvent_t ev_after_dq;
 };
 
 // Each returns cudaSuccess or the launch error.  `stream` is the caller's.

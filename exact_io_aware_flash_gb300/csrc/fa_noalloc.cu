@@ -1,6 +1,6 @@
 // fa_backward_noalloc: the backward pass for callers that cannot allocate
-// device memory.  Its scratch (the D vector and the fp32 dQ accumulator that
-// fa_backward otherwise takes as a caller-provided workspace) lives in one
+// device memory.  Its scratch (the D vector that fa_backward otherwise takes
+// as a caller-provided workspace) lives in one
 // fixed-size array that is part of the library's device image.  It exists
 // only on the library side: the attention method itself has no counterpart.
 #include "../../include/fa.h"

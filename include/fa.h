@@ -84,11 +84,9 @@ FA_API int fa_forward(const void* q, const void* k, const void* v, void* o, floa
                int Hkv, int N, int d, int causal, float scale, int dtype, void* stream);
 
 /*
- * Bytes of device workspace fa_backward needs for these sizes.  Returns 0 if
- * the sizes are invalid.  Layout (offsets in bytes from the workspace base):
- *   [0, a)        D      float32 [B, Hq, N], D_i = sum_c dO_ic * O_ic
- *   [a, a + b)    dQacc  float32 [B, Hq, N, d], unscaled dQ accumulator
- * with a = round_up(4*B*Hq*N, 256) and b = 4*B*Hq*N*d.
+ * Bytes of device workspace fa_backward needs for these sizes: round_up(4 *
+ * B*Hq*N, 256).  Returns 0 if the sizes are invalid.  Layout: D float32
+ * [B, Hq, N] at offset 0, D_i = sum_c dO_ic * O_ic.
  */
 FA_API size_t fa_backward_workspace_size(int B, int Hq, int N, int d);
 
@@ -97,20 +95,21 @@ FA_API size_t fa_backward_workspace_size(int B, int Hq, int N, int d);
  * lse, and dO = dL/dO, writes dq, dk, dv (element type dtype).
  *
  * Steps, all on `stream`:
- *   1. D_i = rowsum(dO_i * O_i) into the workspace, and zero dQacc;
- *   2. per key/value tile, recompute P = exp(scale * Q K^T - LSE) block by
- *      block, and accumulate dV += P^T dO, dS = P * (dO V^T - D),
- *      dK += scale * dS^T Q (summed over the KV head's query group in the
- *      kernel), dQacc += dS K (float32 atomic adds);
- *   3. dq = scale * dQacc converted to dtype.
+ *   1. D_i = rowsum(dO_i * O_i) into the workspace;
+ *   2. per key/value tile, recompute S^T and P^T = exp(scale * K Q^T - LSE)
+ *      block by block and accumulate dV += P^T dO and dK += scale * dS^T Q,
+ *      with dS = P * (dO V^T - D), over all query tiles (and, for grouped
+ *      query attention, over the KV head's query heads) inside one CTA;
+ *   3. per query tile, recompute S and P the same way and accumulate
+ *      dQ += scale * dS K over all key tiles inside one CTA.
  * The gradient is that of the definition: the primer's printed dS omits the
  * -D term and the scale factor, which this library applies (the oracle's
- * finite-difference checks fix the formula).
+ * finite-difference checks fix the formula).  No atomic adds are used: every
+ * sum runs in a fixed order, so dq, dk and dv are bitwise reproducible.
  *
  * workspace: device memory of at least fa_backward_workspace_size() bytes,
  * 256-byte aligned, owned by the caller, not used concurrently by another
- * call.  The dQ accumulation order varies between runs (atomic adds), so dq
- * may differ in the last bits from run to run; dk and dv are deterministic.
+ * call.
  */
 FA_API int fa_backward(const void* q, const void* k, const void* v, const void* o, const float* lse,
                 const void* dO, void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
@@ -122,8 +121,8 @@ FA_API int fa_backward(const void* q, const void* k, const void* v, const void* 
  * method has no counterpart of it.)
  *
  * Same arguments, outputs, errors and asynchrony as fa_backward, minus the
- * workspace: the scratch fa_backward needs (the D vector and the float32 dQ
- * accumulator, fa_backward_workspace_size() bytes) is taken from one
+ * workspace: the scratch fa_backward needs (the D vector,
+ * fa_backward_workspace_size() bytes) is taken from one
  * FA_NOALLOC_SCRATCH_BYTES-byte array compiled into the library's device code,
  * which every GPU that loads the library holds until the process exits.  It is
  * for callers that may not call cudaMalloc or any other allocator: a host
@@ -138,8 +137,8 @@ FA_API int fa_backward(const void* q, const void* k, const void* v, const void* 
  * - The first call on each device looks up the array's device address with
  *   that device current; make that first call before any stream capture.
  * - Every call on a device shares the one array and leaves its contents
- *   behind; each call clears what must start at zero (the dQ accumulator) and
- *   overwrites the rest.  Calls whose GPU work overlaps (different streams, or
+ *   behind; each call overwrites every element it later reads, so nothing
+ *   has to start at zero.  Calls whose GPU work overlaps (different streams, or
  *   different host threads, without ordering between them) race on the array
  *   and give wrong gradients: serialise them.
  * - Calls no cudaMalloc, cudaFree or other allocating routine.
@@ -151,15 +150,16 @@ FA_API int fa_backward_noalloc(const void* q, const void* k, const void* v, cons
                                int dtype, void* stream);
 
 /*
- * Profiling hook for the backward's main kernel.  After this call, every
- * fa_backward issued from the calling host thread records `before` on its stream
- * immediately before launching the main (recomputing) kernel and `after`
- * immediately after it, so cudaEventElapsedTime(before, after) is that kernel's
- * device time.  Both are cudaEvent_t handles passed as void*, created and owned
- * by the caller; pass NULL, NULL to stop.  Thread-local; never synchronises.
- * Returns FA_OK, or FA_ERR_INVALID if exactly one of the two is NULL.
+ * Profiling hook for the backward's two main kernels.  After this call, every
+ * fa_backward issued from the calling host thread records, on its stream,
+ * `before_dkdv` immediately before launching the dK/dV kernel, `before_dq`
+ * between it and the dQ kernel, and `after_dq` immediately after the dQ
+ * kernel; cudaEventElapsedTime between consecutive events is each kernel's
+ * device time.  All are cudaEvent_t handles passed as void*, created and
+ * owned by the caller; pass three NULLs to stop.  Thread-local; never
+ * synchronises.  Returns FA_OK, or FA_ERR_INVALID if only some are NULL.
  */
-FA_API int fa_set_backward_event_hooks(void* before, void* after);
+FA_API int fa_set_backward_event_hooks(void* before_dkdv, void* before_dq, void* after_dq);
 
 /*
  * Synchronises `stream`, then reads and clears the device error word that the
