@@ -316,10 +316,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         issue_s(0);
         issue_dp(0);
       }
+      // Issue order per iteration: dV(it), S^T(it+1), dK(it), dP^T(it+1).  S^T(it+1)
+      // needs only dV(it) finished (it overwrites the P^T columns), so the next
+      // P^T phase can start while this iteration's dS^T is still being computed.
       for (int it = 0; ok && it < n_it; ++it) {
         const int st = it & 1;
         const uint32_t qa = sq + st * L::kTile;
         const uint32_t doa = sdo + st * L::kTile;
+        const bool more = it + 1 < n_it;
+        const int st1 = (it + 1) & 1;
         // dV += P^T dO_i   (P^T: 16-bit pairs over the first half of the S^T columns)
         if (!(ok = mbar_wait(&bar[KB_PREADY], it & 1, abort_flag, err))) break;
         tc_fence_after();
@@ -328,6 +333,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ts(tmem + kColDV, tmem + kColS + ks * 8, mnmajor_desc(doa, ks), kIdKV,
                  (it > 0 || ks > 0) ? 1u : 0u);
         mma_commit(&bar[KB_DVDONE]);
+        if (more) {
+          if (!(ok = mbar_wait(&bar[KB_QFULL + st1], ((it + 1) >> 1) & 1, abort_flag, err))) break;
+          if (!(ok = mbar_wait(&bar[KB_DVDONE], it & 1, abort_flag, err))) break;
+          tc_fence_after();
+          issue_s(st1);
+        }
         // dK += dS^T Q_i   (dS^T: 16-bit pairs over the first half of the dP^T columns)
         if (!(ok = mbar_wait(&bar[KB_DSREADY], it & 1, abort_flag, err))) break;
         tc_fence_after();
@@ -337,13 +348,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                  (it > 0 || ks > 0) ? 1u : 0u);
         mma_commit(&bar[KB_DKDONE]);
         mma_commit(&bar[KB_QEMPTY + st]);
-        if (it + 1 < n_it) {
-          const int st1 = (it + 1) & 1;
-          if (!(ok = mbar_wait(&bar[KB_QFULL + st1], ((it + 1) >> 1) & 1, abort_flag, err))) break;
-          // S^T(it+1) overwrites the columns dV(it) reads; dP^T(it+1) those dK(it) reads.
-          if (!(ok = mbar_wait(&bar[KB_DVDONE], it & 1, abort_flag, err))) break;
-          tc_fence_after();
-          issue_s(st1);
+        if (more) {
+          // dP^T(it+1) overwrites the dS^T columns dK(it) reads.
           if (!(ok = mbar_wait(&bar[KB_DKDONE], it & 1, abort_flag, err))) break;
           tc_fence_after();
           issue_dp(st1);
@@ -456,13 +462,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------ dQ
+// K_j is read by S(j) and by dQ(j), the last MMA of an iteration, so its stage
+// frees late; three stages let the load of K_{j+2} overlap dQ(j).  V_j is read
+// only by dP(j) and frees early: two stages.
+constexpr int kDqKStages = 3;
+
 template <int D>
 struct DqSmem {
   static constexpr int kTile = kBlk * D * 2;
   static constexpr int kQ = 0;
   static constexpr int kdO = kQ + kTile;
-  static constexpr int kK = kdO + kTile;       // 2 stages
-  static constexpr int kV = kK + 2 * kTile;    // 2 stages
+  static constexpr int kK = kdO + kTile;                 // kDqKStages stages
+  static constexpr int kV = kK + kDqKStages * kTile;     // 2 stages
   static constexpr int kBar = kV + 2 * kTile;
   static constexpr int kBytes = kBar + 256;
   static constexpr int kAlloc = kBytes + 1024;
@@ -470,18 +481,18 @@ struct DqSmem {
 
 enum DqBars {
   QB_Q = 0,       // Q_i, dO_i
-  QB_KFULL = 1,   // +stage
-  QB_KEMPTY = 3,  // +stage
-  QB_VFULL = 5,   // +stage
-  QB_VEMPTY = 7,  // +stage
-  QB_SFULL = 9,
-  QB_DPFULL = 10,
-  QB_SFREE = 11,   // S read into registers (4 warps)
-  QB_DPFREE = 12,  // dP read (4 warps)
-  QB_DSREADY = 13, // dS written to TMEM (4 warps)
-  QB_DQDONE = 14,  // dQ MMA done: dS columns free
-  QB_FINAL = 15,
-  QB_N = 16
+  QB_KFULL = 1,   // +stage (3)
+  QB_KEMPTY = 4,  // +stage (3)
+  QB_VFULL = 7,   // +stage (2)
+  QB_VEMPTY = 9,  // +stage (2)
+  QB_SFULL = 11,
+  QB_DPFULL = 12,
+  QB_SFREE = 13,   // S read into registers (4 warps)
+  QB_DPFREE = 14,  // dP read (4 warps)
+  QB_DSREADY = 15, // dS written to TMEM (4 warps)
+  QB_DQDONE = 16,  // dQ MMA done: dS columns free
+  QB_FINAL = 17,
+  QB_N = 18
 };
 
 template <int D, bool BF16>
@@ -544,31 +555,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(smem + L::kQ + a * kAtomBytes, &tm_q, &bar[QB_Q], a * 64, i * kBlk, bhq, pol_q);
         tma_load_3d(smem + L::kdO + a * kAtomBytes, &tm_do, &bar[QB_Q], a * 64, i * kBlk, bhq, pol_q);
       }
-      int issued = 0;
+      int kissued = 0, vissued = 0;
       for (int jj = 0; jj < n_j; ++jj) {
-        const int st = jj & 1;
-        const uint32_t ph = (jj >> 1) & 1;
-        if (!mbar_wait(&bar[QB_KEMPTY + st], ph ^ 1, abort_flag, err)) break;
-        mbar_expect_tx(&bar[QB_KFULL + st], L::kTile);
+        const int sk = jj % kDqKStages;
+        const uint32_t pk = (jj / kDqKStages) & 1;
+        const int sv = jj & 1;
+        const uint32_t pv = (jj >> 1) & 1;
+        if (!mbar_wait(&bar[QB_KEMPTY + sk], pk ^ 1, abort_flag, err)) break;
+        mbar_expect_tx(&bar[QB_KFULL + sk], L::kTile);
         for (int a = 0; a < kAtoms; ++a)
-          tma_load_3d(smem + L::kK + st * L::kTile + a * kAtomBytes, &tm_k, &bar[QB_KFULL + st],
+          tma_load_3d(smem + L::kK + sk * L::kTile + a * kAtomBytes, &tm_k, &bar[QB_KFULL + sk],
                       a * 64, jj * kBlk, kvh, pol_kv);
-        if (!mbar_wait(&bar[QB_VEMPTY + st], ph ^ 1, abort_flag, err)) {
-          issued = 2 * jj + 1;
-          break;
-        }
-        mbar_expect_tx(&bar[QB_VFULL + st], L::kTile);
+        kissued = jj + 1;
+        if (!mbar_wait(&bar[QB_VEMPTY + sv], pv ^ 1, abort_flag, err)) break;
+        mbar_expect_tx(&bar[QB_VFULL + sv], L::kTile);
         for (int a = 0; a < kAtoms; ++a)
-          tma_load_3d(smem + L::kV + st * L::kTile + a * kAtomBytes, &tm_v, &bar[QB_VFULL + st],
+          tma_load_3d(smem + L::kV + sv * L::kTile + a * kAtomBytes, &tm_v, &bar[QB_VFULL + sv],
                       a * 64, jj * kBlk, kvh, pol_kv);
-        issued = 2 * jj + 2;
+        vissued = jj + 1;
       }
       if (*abort_flag) {
         drain_wait(&bar[QB_Q], 0);
-        for (int x = (issued > 4 ? issued - 4 : 0); x < issued; ++x) {
-          const int jj = x >> 1, st = jj & 1;
-          drain_wait(&bar[((x & 1) ? QB_VFULL : QB_KFULL) + st], (jj >> 1) & 1);
-        }
+        for (int jj = (kissued > kDqKStages ? kissued - kDqKStages : 0); jj < kissued; ++jj)
+          drain_wait(&bar[QB_KFULL + jj % kDqKStages], (jj / kDqKStages) & 1);
+        for (int jj = (vissued > 2 ? vissued - 2 : 0); jj < vissued; ++jj)
+          drain_wait(&bar[QB_VFULL + (jj & 1)], (jj >> 1) & 1);
       }
     }
   } else if (run && warp == 5) {
@@ -580,20 +591,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t sdo = smem_u32(smem + L::kdO);
       const uint32_t sk = smem_u32(smem + L::kK);
       const uint32_t sv = smem_u32(smem + L::kV);
-      auto issue_s = [&](int st) {  // S = Q_i K_j^T
-        const uint32_t ka = sk + st * L::kTile;
+      auto issue_s = [&](int stk) {  // S = Q_i K_j^T
+        const uint32_t ka = sk + stk * L::kTile;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks)
           mma_ss(tmem + kColS, kmajor_desc(sq, ks), kmajor_desc(ka, ks), kIdS, ks > 0);
         mma_commit(&bar[QB_SFULL]);
       };
-      auto issue_dp = [&](int st) {  // dP = dO_i V_j^T; V_j is free again once this completes
-        const uint32_t va = sv + st * L::kTile;
+      auto issue_dp = [&](int stv) {  // dP = dO_i V_j^T; V_j is free again once this completes
+        const uint32_t va = sv + stv * L::kTile;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks)
           mma_ss(tmem + kColDP, kmajor_desc(sdo, ks), kmajor_desc(va, ks), kIdS, ks > 0);
         mma_commit(&bar[QB_DPFULL]);
-        mma_commit(&bar[QB_VEMPTY + st]);
+        mma_commit(&bar[QB_VEMPTY + stv]);
       };
       bool ok = mbar_wait(&bar[QB_Q], 0, abort_flag, err) &&
                 mbar_wait(&bar[QB_KFULL], 0, abort_flag, err);
@@ -607,30 +618,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       for (int jj = 0; ok && jj < n_j; ++jj) {
-        const int st = jj & 1;
+        const int stk = jj % kDqKStages;
         if (jj + 1 < n_j) {
-          const int st1 = (jj + 1) & 1;
-          const uint32_t ph1 = ((jj + 1) >> 1) & 1;
+          const int stk1 = (jj + 1) % kDqKStages;
+          const uint32_t phk1 = ((jj + 1) / kDqKStages) & 1;
+          const int stv1 = (jj + 1) & 1;
+          const uint32_t phv1 = ((jj + 1) >> 1) & 1;
           // S(j+1) may start once S(j) has been read out of TMEM; dP(j+1) once dP(j) has.
-          if (!(ok = mbar_wait(&bar[QB_KFULL + st1], ph1, abort_flag, err))) break;
+          if (!(ok = mbar_wait(&bar[QB_KFULL + stk1], phk1, abort_flag, err))) break;
           if (!(ok = mbar_wait(&bar[QB_SFREE], jj & 1, abort_flag, err))) break;
           tc_fence_after();
-          issue_s(st1);
-          if (!(ok = mbar_wait(&bar[QB_VFULL + st1], ph1, abort_flag, err))) break;
+          issue_s(stk1);
+          if (!(ok = mbar_wait(&bar[QB_VFULL + stv1], phv1, abort_flag, err))) break;
           if (!(ok = mbar_wait(&bar[QB_DPFREE], jj & 1, abort_flag, err))) break;
           tc_fence_after();
-          issue_dp(st1);
+          issue_dp(stv1);
         }
         // dQ += dS K_j   (dS: 16-bit pairs in its own TMEM columns; K_j as an MN-major B)
         if (!(ok = mbar_wait(&bar[QB_DSREADY], jj & 1, abort_flag, err))) break;
         tc_fence_after();
-        const uint32_t ka = sk + st * L::kTile;
+        const uint32_t ka = sk + stk * L::kTile;
 #pragma unroll
         for (int ks = 0; ks < kBlk / 16; ++ks)
           mma_ts(tmem + kColDQ, tmem + kColDS + ks * 8, mnmajor_desc(ka, ks), kIdQ,
                  (jj > 0 || ks > 0) ? 1u : 0u);
         mma_commit(&bar[QB_DQDONE]);
-        mma_commit(&bar[QB_KEMPTY + st]);
+        mma_commit(&bar[QB_KEMPTY + stk]);
       }
       mma_commit(&bar[QB_FINAL]);
       drain_wait(&bar[QB_FINAL], 0);
@@ -678,22 +691,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
 #pragma unroll
-      for (int c = 0; c < kBlk; c += 32) {
-        uint32_t dpv[32];
-        tmem_ld32(tP + c, dpv);
+      for (int h = 0; h < kBlk; h += 64) {  // two TMEM round trips of 64 columns
+        uint32_t dpv[64];
+        tmem_ld32(tP + h, dpv);
+        tmem_ld32(tP + h + 32, dpv + 32);
         tmem_ld_wait();
-        reg_fence<32>(dpv);
-        uint32_t dsw[16];
+        reg_fence<64>(dpv);
+        if (h + 64 == kBlk) {  // dP(j) fully read: dP(j+1) may overwrite it
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bar[QB_DPFREE]);
+        }
 #pragma unroll
-        for (int e = 0; e < 16; ++e)
-          dsw[e] = pack2<BF16>(p[c + 2 * e] * (__uint_as_float(dpv[2 * e]) - dq_d),
-                               p[c + 2 * e + 1] * (__uint_as_float(dpv[2 * e + 1]) - dq_d));
-        tmem_st16(tDS + c / 2, dsw);
+        for (int c = 0; c < 64; c += 32) {
+          uint32_t dsw[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            dsw[e] = pack2<BF16>(p[h + c + 2 * e] * (__uint_as_float(dpv[c + 2 * e]) - dq_d),
+                                 p[h + c + 2 * e + 1] * (__uint_as_float(dpv[c + 2 * e + 1]) - dq_d));
+          tmem_st16(tDS + (h + c) / 2, dsw);
+        }
       }
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bar[QB_DPFREE]);
       if (lane == 0) mbar_arrive(&bar[QB_DSREADY]);
     }
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bar[QB_FINAL], 0, abort_flag, err));

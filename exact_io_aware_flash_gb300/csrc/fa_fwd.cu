@@ -13,9 +13,9 @@
 //   warp 8      TMA producer: Q tiles once, then K_j and V_j through two
 //               2-stage shared-memory rings (128-byte swizzle, 3-D tensor maps
 //               over [B*H, N, d] so ragged tails are zero-filled).
-//   warp 9      MMA issuer (one thread): S_X = Q_X K_j^T into Tensor Memory,
-//               O_X += P_X V_j with P_X read from Tensor Memory (A operand) and
-//               V_j from shared memory as an MN-major B operand.
+//   warps 9-10  MMA issuers, one thread per query tile X: S_X = Q_X K_j^T into
+//               Tensor Memory, O_X += P_X V_j with P_X read from Tensor Memory
+//               (A operand) and V_j from shared memory as an MN-major B operand.
 //   warps 0-3   softmax for query tile A, warps 4-7 for tile B: thread t owns
 //               row t (TMEM lane t); exp2 with the scale folded in; P written
 //               back to TMEM as 16-bit pairs over the first half of S.
@@ -42,31 +42,34 @@ namespace {
 constexpr int kBM = 128;           // query rows per tile
 constexpr int kBN = 128;           // keys per tile
 constexpr int kAtomBytes = 16384;  // 128 rows x 128 bytes: 64 columns of one 16-bit tile
-constexpr int kThreads = 320;      // 10 warps
-constexpr int kStages = 2;
+constexpr int kThreads = 352;      // 11 warps
+// The two query tiles run half a period apart, so K_j is released by the
+// later tile; a third K stage lets K_{j+2} load while that tile finishes.
+constexpr int kKStages = 3;
+constexpr int kVStages = 2;
 
 template <int D>
 struct FwdSmem {
   static constexpr int kTile = kBM * D * 2;  // bytes of one 128 x D 16-bit tile
   static constexpr int kQ = 0;               // 2 query tiles
-  static constexpr int kK = kQ + 2 * kTile;  // K ring
-  static constexpr int kV = kK + kStages * kTile;
-  static constexpr int kBar = kV + kStages * kTile;
+  static constexpr int kK = kQ + 2 * kTile;  // K ring, kKStages
+  static constexpr int kV = kK + kKStages * kTile;  // V ring, kVStages
+  static constexpr int kBar = kV + kVStages * kTile;
   static constexpr int kBytes = kBar + 256;
   static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
 };
 
 enum Bars {
   BQ = 0,
-  BKFULL = 1,   // +stage
-  BKEMPTY = 3,  // +stage
-  BVFULL = 5,
-  BVEMPTY = 7,
-  BSFULL = 9,   // +tile
-  BPFULL = 11,  // +tile
-  BODONE = 13,  // +tile
-  BFINAL = 15,
-  NBARS = 16
+  BKFULL = 1,    // +stage (3)
+  BKEMPTY = 4,   // +stage (3), one arrival per MMA issuer
+  BVFULL = 7,    // +stage (2)
+  BVEMPTY = 9,   // +stage (2), one arrival per MMA issuer
+  BSFULL = 11,   // +tile
+  BPFULL = 13,   // +tile
+  BODONE = 15,   // +tile
+  BFINAL = 17,   // +tile
+  NBARS = 19
 };
 
 template <bool BF16>
@@ -121,7 +124,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nKV = nA > nB ? nA : nB;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < NBARS; ++i) mbar_init(&bar[i], (i == BPFULL || i == BPFULL + 1) ? 4 : 1);
+    for (int i = 0; i < NBARS; ++i) {
+      uint32_t cnt = 1;
+      if (i == BPFULL || i == BPFULL + 1) cnt = 4;
+      if ((i >= BKEMPTY && i < BKEMPTY + kKStages) || (i >= BVEMPTY && i < BVEMPTY + kVStages)) cnt = 2;
+      mbar_init(&bar[i], cnt);
+    }
     *abort_flag = (*reinterpret_cast<volatile int*>(err) != kDevErrNone) ? 1 : 0;
     fence_mbar_init();
   }
@@ -149,110 +157,115 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(smem + L::kQ + L::kTile + a * kAtomBytes, &tm_q, &bar[BQ], a * 64, tB * kBM,
                       bh, pol_q);
       }
-      int issued = 0;
+      int kissued = 0, vissued = 0;
       for (int j = 0; j < nKV; ++j) {
-        const int st = j & 1;
-        const uint32_t ph = (j >> 1) & 1;
-        if (!mbar_wait(&bar[BKEMPTY + st], ph ^ 1, abort_flag, err)) break;
-        mbar_expect_tx(&bar[BKFULL + st], L::kTile);
+        const int sk = j % kKStages;
+        const uint32_t pk = (j / kKStages) & 1;
+        const int sv = j % kVStages;
+        const uint32_t pv = (j / kVStages) & 1;
+        if (!mbar_wait(&bar[BKEMPTY + sk], pk ^ 1, abort_flag, err)) break;
+        mbar_expect_tx(&bar[BKFULL + sk], L::kTile);
         for (int a = 0; a < kAtoms; ++a)
-          tma_load_3d(smem + L::kK + st * L::kTile + a * kAtomBytes, &tm_k, &bar[BKFULL + st],
+          tma_load_3d(smem + L::kK + sk * L::kTile + a * kAtomBytes, &tm_k, &bar[BKFULL + sk],
                       a * 64, j * kBN, kvh, pol_kv);
-        if (!mbar_wait(&bar[BVEMPTY + st], ph ^ 1, abort_flag, err)) {
-          issued = 2 * j + 1;
-          break;
-        }
-        mbar_expect_tx(&bar[BVFULL + st], L::kTile);
+        kissued = j + 1;
+        if (!mbar_wait(&bar[BVEMPTY + sv], pv ^ 1, abort_flag, err)) break;
+        mbar_expect_tx(&bar[BVFULL + sv], L::kTile);
         for (int a = 0; a < kAtoms; ++a)
-          tma_load_3d(smem + L::kV + st * L::kTile + a * kAtomBytes, &tm_v, &bar[BVFULL + st],
+          tma_load_3d(smem + L::kV + sv * L::kTile + a * kAtomBytes, &tm_v, &bar[BVFULL + sv],
                       a * 64, j * kBN, kvh, pol_kv);
-        issued = 2 * j + 2;
+        vissued = j + 1;
       }
       if (*abort_flag) {
         // Let every copy already issued land before shared memory is released.
         drain_wait(&bar[BQ], 0);
-        for (int i = (issued > 4 ? issued - 4 : 0); i < issued; ++i) {
-          const int j = i >> 1, st = j & 1;
-          drain_wait(&bar[((i & 1) ? BVFULL : BKFULL) + st], (j >> 1) & 1);
-        }
+        for (int j = (kissued > kKStages ? kissued - kKStages : 0); j < kissued; ++j)
+          drain_wait(&bar[BKFULL + j % kKStages], (j / kKStages) & 1);
+        for (int j = (vissued > kVStages ? vissued - kVStages : 0); j < vissued; ++j)
+          drain_wait(&bar[BVFULL + j % kVStages], (j / kVStages) & 1);
       }
     }
-  } else if (run && warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (run && (warp == 9 || warp == 10)) {
+    // ------------------------------------------------------------ MMA issuers
+    // One issuing thread per query tile: a thread blocks while the tensor core
+    // accepts its MMAs, and with one issuer per tile that blocking never holds
+    // up the other tile's chain.  Each tile runs S(j), softmax(j), PV(j),
+    // S(j+1), ...; S(j+1) overwrites the columns PV(j) reads P from, so it is
+    // issued once PV(j) has completed (tcgen05 orders MMAs only for the same
+    // accumulator).  K_j and V_j are released when both tiles are done with
+    // them: the empty barriers count one arrival per issuer.
     if (lane == 0) {
+      const int X = warp - 9;
+      const int nX = X ? nB : nA;
       constexpr uint32_t kIdS = idesc_f16(kBM, kBN, BF16, false, false);
       constexpr uint32_t kIdO = idesc_f16(kBM, D, BF16, false, true);
-      const uint32_t sq = smem_u32(smem + L::kQ);
+      const uint32_t qa = smem_u32(smem + L::kQ) + X * L::kTile;
       const uint32_t sk = smem_u32(smem + L::kK);
       const uint32_t sv = smem_u32(smem + L::kV);
+      const uint32_t tS = tmem + X * 128;
+      const uint32_t tO = tmem + 256 + X * 128;
 
-      auto issue_s = [&](int X, int st) {
-        const uint32_t dt = tmem + X * 128;
-        const uint32_t qa = sq + X * L::kTile;
-        const uint32_t ka = sk + st * L::kTile;
+      auto issue_s = [&](int stk) {  // S_X = Q_X K_j^T
+        const uint32_t ka = sk + stk * L::kTile;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t off = (ks >> 2) * kAtomBytes + (ks & 3) * 32;
-          mma_ss(dt, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), kIdS,
+          mma_ss(tS, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), kIdS,
                  ks > 0);
         }
         mma_commit(&bar[BSFULL + X]);
+        mma_commit(&bar[BKEMPTY + stk]);
       };
-      auto issue_pv = [&](int X, int st, int j) {
-        const uint32_t dt = tmem + 256 + X * 128;
-        const uint32_t pt = tmem + X * 128;
-        const uint32_t va = sv + st * L::kTile;
+      auto issue_pv = [&](int stv, int j) {
+        const uint32_t va = sv + stv * L::kTile;
 #pragma unroll
         for (int ks = 0; ks < kBN / 16; ++ks)
-          mma_ts(dt, pt + ks * 8, sdesc_sw128(va + ks * 2048, kAtomBytes, 1024), kIdO,
+          mma_ts(tO, tS + ks * 8, sdesc_sw128(va + ks * 2048, kAtomBytes, 1024), kIdO,
                  (j > 0 || ks > 0) ? 1u : 0u);
         mma_commit(&bar[BODONE + X]);
+        mma_commit(&bar[BVEMPTY + stv]);
       };
 
-      bool ok = mbar_wait(&bar[BQ], 0, abort_flag, err) &&
-                mbar_wait(&bar[BKFULL], 0, abort_flag, err);
-      if (ok) {
-        tc_fence_after();
-        issue_s(0, 0);
-        if (nB > 0) issue_s(1, 0);
-        mma_commit(&bar[BKEMPTY]);
+      bool ok = true;
+      if (nX > 0) {
+        ok = mbar_wait(&bar[BQ], 0, abort_flag, err) && mbar_wait(&bar[BKFULL], 0, abort_flag, err);
+        if (ok) {
+          tc_fence_after();
+          issue_s(0);
+        }
       }
-      for (int j = 0; ok && j < nKV; ++j) {
-        const int st = j & 1;
-        const uint32_t ph = (j >> 1) & 1;
-        if (!(ok = mbar_wait(&bar[BVFULL + st], ph, abort_flag, err))) break;
-        if (j < nA) {
-          if (!(ok = mbar_wait(&bar[BPFULL], j & 1, abort_flag, err))) break;
+      for (int j = 0; ok && j < nX; ++j) {
+        const int stv = j % kVStages;
+        if (!(ok = mbar_wait(&bar[BVFULL + stv], (j / kVStages) & 1, abort_flag, err))) break;
+        if (!(ok = mbar_wait(&bar[BPFULL + X], j & 1, abort_flag, err))) break;
+        tc_fence_after();
+        issue_pv(stv, j);
+        if (j + 1 < nX) {
+          const int stk1 = (j + 1) % kKStages;
+          if (!(ok = mbar_wait(&bar[BKFULL + stk1], ((j + 1) / kKStages) & 1, abort_flag, err))) break;
+          if (!(ok = mbar_wait(&bar[BODONE + X], j & 1, abort_flag, err))) break;
           tc_fence_after();
-          issue_pv(0, st, j);
+          issue_s(stk1);
         }
-        if (j < nB) {
-          if (!(ok = mbar_wait(&bar[BPFULL + 1], j & 1, abort_flag, err))) break;
-          tc_fence_after();
-          issue_pv(1, st, j);
-        }
-        mma_commit(&bar[BVEMPTY + st]);
-        if (j + 1 < nKV) {
-          const int st1 = (j + 1) & 1;
-          const uint32_t ph1 = ((j + 1) >> 1) & 1;
-          if (!(ok = mbar_wait(&bar[BKFULL + st1], ph1, abort_flag, err))) break;
-          // S_X(j+1) overwrites the columns P_X(j) was read from: wait for PV_X(j).
-          if (j + 1 < nA) {
-            if (!(ok = mbar_wait(&bar[BODONE], j & 1, abort_flag, err))) break;
-            tc_fence_after();
-            issue_s(0, st1);
-          }
-          if (j + 1 < nB) {
-            if (!(ok = mbar_wait(&bar[BODONE + 1], j & 1, abort_flag, err))) break;
-            tc_fence_after();
-            issue_s(1, st1);
-          }
-          mma_commit(&bar[BKEMPTY + st1]);
-        }
+      }
+      // Key tiles this query tile does not visit still need this issuer's
+      // release.  Its arrival for a use of a stage may only come after that
+      // stage's previous use has been released by both issuers.
+      for (int j = nX; ok && j < nKV; ++j) {
+        const int stk = j % kKStages;
+        const int stv = j % kVStages;
+        if (j >= kKStages && !(ok = mbar_wait(&bar[BKEMPTY + stk], ((j / kKStages) - 1) & 1,
+                                              abort_flag, err)))
+          break;
+        if (j >= kVStages && !(ok = mbar_wait(&bar[BVEMPTY + stv], ((j / kVStages) - 1) & 1,
+                                              abort_flag, err)))
+          break;
+        mbar_arrive(&bar[BKEMPTY + stk]);
+        mbar_arrive(&bar[BVEMPTY + stv]);
       }
       // Every MMA this thread issued has completed before TMEM is released.
-      mma_commit(&bar[BFINAL]);
-      drain_wait(&bar[BFINAL], 0);
+      mma_commit(&bar[BFINAL + X]);
+      drain_wait(&bar[BFINAL + X], 0);
     }
   } else if (run && warp < 8) {
     // ------------------------------------------------------------ softmax
@@ -270,7 +283,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sfac = pos_scale ? scale_log2 : 1.0f;
     bool ok = true;
     for (int j = 0; j < nX; ++j) {
-      ok = __all_sync(0xffffffffu, mbar_wait(&bar[BSFULL + X], j & 1, abort_flag, err));
+      // The two tiles' softmaxes take turns -- A(0), B(0), A(1), B(1), ... -- so
+      // each runs alone on the SM's ALUs while the tensor core works on the
+      // other tile.  A(j) follows B(j-1); B(j) follows A(j) where tile A has one.
+      bool turn = true;
+      if (X == 0 && j > 0 && nB > 0) turn = mbar_wait(&bar[BPFULL + 1], (j - 1) & 1, abort_flag, err);
+      if (X == 1 && j < nA) turn = mbar_wait(&bar[BPFULL], j & 1, abort_flag, err);
+      ok = __all_sync(0xffffffffu, turn && mbar_wait(&bar[BSFULL + X], j & 1, abort_flag, err));
       if (!ok) break;
       tc_fence_after();
       // x holds the scores as raw bits: s * scale * log2(e) after the first pass.
