@@ -118,9 +118,8 @@ int check_common(int B, int Hq, int Hkv, int N, int d, float scale, int dtype) {
   if (d != 64 && d != 128) return fail(FA_ERR_UNSUPPORTED, "head dimension d=%d (supported: 64, 128)", d);
   if (dtype != FA_DTYPE_FP16 && dtype != FA_DTYPE_BF16)
     return fail(FA_ERR_UNSUPPORTED, "dtype %d (supported: FA_DTYPE_FP16, FA_DTYPE_BF16)", dtype);
-  // grid.y carries the (batch, head) index of the forward and backward grids.
-  if ((long long)B * Hq > 65535)
-    return fail(FA_ERR_UNSUPPORTED, "B*Hq=%lld exceeds 65535", (long long)B * Hq);
+  // One-dimensional grids enumerate (head, 128-row tile) work items; the TMA
+  // head coordinate and row indices are 32-bit.
   if ((long long)B * Hq * N > 0x7fffffffLL) return fail(FA_ERR_UNSUPPORTED, "B*Hq*N exceeds 2^31-1");
   return FA_OK;
 }

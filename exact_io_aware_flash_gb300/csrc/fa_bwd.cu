@@ -49,6 +49,7 @@ constexpr int kBlk = 128;          // rows per tile (keys and queries)
 constexpr int kAtomBytes = 16384;  // 128 rows x 128 bytes
 constexpr int kThreads = 192;
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kHeadGroup = 16;  // heads scheduled together (their operands stay in L2)
 
 template <bool BF16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
@@ -186,8 +187,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                        const float* __restrict__ lse, const float* __restrict__ Drow,
-                       void* __restrict__ dk_out, void* __restrict__ dv_out, int Hq, int Hkv, int N,
-                       int causal, float scale, int* err) {
+                       void* __restrict__ dk_out, void* __restrict__ dv_out, int heads, int Hq,
+                       int Hkv, int N, int causal, float scale, int* err) {
   using L = DkdvSmem<D>;
   constexpr int kAtoms = D / 64;
   extern __shared__ uint8_t smem_raw[];
@@ -198,14 +199,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // All key tiles of one KV head run side by side (that head's Q and dO stay
-  // in L2); within a head j = 0, the most work under causal masking, first.
-  const int j = blockIdx.x;
-  const int bkv = blockIdx.y;  // b * Hkv + hkv
+  const int T = (N + kBlk - 1) / kBlk;
+  // Groups of KV heads whose Q and dO stay in L2; within a group the key tiles
+  // with the most work under causal masking (small j) first.
+  const WorkItem wi = grouped_heavy_first(blockIdx.x, heads, T, kHeadGroup);
+  const int j = wi.rank;
+  const int bkv = wi.head;  // b * Hkv + hkv
   const int b = bkv / Hkv;
   const int hkv = bkv % Hkv;
   const int group = Hq / Hkv;
-  const int T = (N + kBlk - 1) / kBlk;
   const int i0 = causal ? j : 0;
   const int n_i = T - i0;
   const int n_it = group * n_i;
@@ -500,8 +502,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                      const float* __restrict__ lse, const float* __restrict__ Drow,
-                     void* __restrict__ dq_out, int Hq, int Hkv, int N, int causal, float scale,
-                     int* err) {
+                     void* __restrict__ dq_out, int heads, int Hq, int Hkv, int N, int causal,
+                     float scale, int* err) {
   using L = DqSmem<D>;
   constexpr int kAtoms = D / 64;
   extern __shared__ uint8_t smem_raw[];
@@ -513,10 +515,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int T = (N + kBlk - 1) / kBlk;
-  // Query tiles of one head side by side (its K, V stay in L2); the tile with
-  // the most key tiles under causal masking first.
-  const int i = T - 1 - static_cast<int>(blockIdx.x);
-  const int bhq = blockIdx.y;  // b * Hq + hq
+  // Groups of query heads whose K and V stay in L2; within a group the query
+  // tiles with the most key tiles under causal masking (large i) first.
+  const WorkItem wi = grouped_heavy_first(blockIdx.x, heads, T, kHeadGroup);
+  const int i = T - 1 - wi.rank;
+  const int bhq = wi.head;  // b * Hq + hq
   const int b = bhq / Hq;
   const int hq = bhq % Hq;
   const int kvh = b * Hkv + hq / (Hq / Hkv);
@@ -762,14 +765,14 @@ cudaError_t launch_bwd_t(const AttnShape& s, const BwdArgs& a, cudaStream_t stre
     return e;
 
   if (a.ev_before_dkdv && (e = cudaEventRecord(a.ev_before_dkdv, stream)) != cudaSuccess) return e;
-  kdkdv<<<dim3(static_cast<unsigned>(T), static_cast<unsigned>(s.B * s.Hkv)), kThreads, smem_kv,
-          stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.lse, a.D, a.dk, a.dv, s.Hq, s.Hkv, s.N,
-                    s.causal, s.scale, a.err);
+  kdkdv<<<dim3(static_cast<unsigned>(T * s.B * s.Hkv)), kThreads, smem_kv, stream>>>(
+      a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.lse, a.D, a.dk, a.dv, s.B * s.Hkv, s.Hq, s.Hkv, s.N,
+      s.causal, s.scale, a.err);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (a.ev_before_dq && (e = cudaEventRecord(a.ev_before_dq, stream)) != cudaSuccess) return e;
-  kdq<<<dim3(static_cast<unsigned>(T), static_cast<unsigned>(s.B * s.Hq)), kThreads, smem_q,
-        stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.lse, a.D, a.dq, s.Hq, s.Hkv, s.N, s.causal,
-                  s.scale, a.err);
+  kdq<<<dim3(static_cast<unsigned>(T * s.B * s.Hq)), kThreads, smem_q, stream>>>(
+      a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.lse, a.D, a.dq, s.B * s.Hq, s.Hq, s.Hkv, s.N, s.causal,
+      s.scale, a.err);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (a.ev_after_dq && (e = cudaEventRecord(a.ev_after_dq, stream)) != cudaSuccess) return e;
   return cudaSuccess;

@@ -46,6 +46,7 @@ constexpr int kThreads = 352;      // 11 warps
 // The two query tiles run half a period apart, so K_j is released by the
 // later tile; a third K stage lets K_{j+2} load while that tile finishes.
 constexpr int kKStages = 3;
+constexpr int kHeadGroup = 16;  // heads scheduled together (their K, V: 32 MB at N=4096)
 constexpr int kVStages = 2;
 
 template <int D>
@@ -96,7 +97,7 @@ template <int D, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, void* __restrict__ out,
-                  float* __restrict__ lse_out, int Hq, int Hkv, int N, int causal,
+                  float* __restrict__ lse_out, int heads, int Hq, int Hkv, int N, int causal,
                   float scale_log2, int* err) {
   using L = FwdSmem<D>;
   constexpr int kAtoms = D / 64;
@@ -109,14 +110,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // The query-tile pairs of one head run side by side so that head's K and V
-  // stay in L2; within a head the heaviest causal pairs are launched first.
-  const int pair = gridDim.x - 1 - blockIdx.x;
-  const int bh = blockIdx.y;  // b * Hq + h
+  const int T = (N + kBM - 1) / kBM;
+  const int pairs = (T + 1) / 2;
+  // Groups of heads whose K and V stay in L2; heaviest causal pairs first.
+  const WorkItem wi = grouped_heavy_first(blockIdx.x, heads, pairs, kHeadGroup);
+  const int pair = pairs - 1 - wi.rank;
+  const int bh = wi.head;  // b * Hq + h
   const int h = bh % Hq;
   const int b = bh / Hq;
   const int kvh = b * Hkv + h / (Hq / Hkv);
-  const int T = (N + kBM - 1) / kBM;
   const int tA = 2 * pair, tB = 2 * pair + 1;
   const bool hasB = tB < T;
   const int nA = causal ? tA + 1 : T;
@@ -417,10 +419,10 @@ cudaError_t launch_fwd_t(const AttnShape& s, const FwdArgs& a, cudaStream_t stre
   if (e != cudaSuccess) return e;
   const int T = (s.N + kBM - 1) / kBM;
   const int pairs = (T + 1) / 2;
-  dim3 grid(static_cast<unsigned>(pairs), static_cast<unsigned>(s.B * s.Hq));
+  dim3 grid(static_cast<unsigned>(pairs * s.B * s.Hq));  // (head, pair) work items
   const float scale_log2 = s.scale * 1.4426950408889634f;
-  kern<<<grid, kThreads, smem, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.o, a.lse, s.Hq, s.Hkv, s.N,
-                                         s.causal, scale_log2, a.err);
+  kern<<<grid, kThreads, smem, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.o, a.lse, s.B * s.Hq, s.Hq,
+                                         s.Hkv, s.N, s.causal, scale_log2, a.err);
   return cudaGetLastError();
 }
 

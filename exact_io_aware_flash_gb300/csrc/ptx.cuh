@@ -321,6 +321,29 @@ __device__ __forceinline__ float4 lds128_ordered(const void* p) {
   return v;
 }
 
+// ---------------------------------------------------------------- scheduling
+// Maps a linear block index onto (head, rank) for `heads` x `ranks` work items
+// whose cost falls with the rank (rank 0 is the heaviest).  Heads are taken in
+// groups of `group` so that the group's operands stay in L2; within a group the
+// items run heaviest first across all the group's heads, so the grid ends on
+// the lightest items instead of on the heaviest items of the last heads.
+struct WorkItem {
+  int head;
+  int rank;
+};
+__device__ __forceinline__ WorkItem grouped_heavy_first(int linear, int heads, int ranks,
+                                                        int group) {
+  const int per_group = group * ranks;
+  const int g = linear / per_group;
+  const int r = linear - g * per_group;
+  const int rem = heads - g * group;
+  const int gh = rem < group ? rem : group;  // heads in this (possibly last) group
+  WorkItem w;
+  w.rank = r / gh;
+  w.head = g * group + (r - w.rank * gh);
+  return w;
+}
+
 // ---------------------------------------------------------------- math
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
