@@ -49,7 +49,6 @@ constexpr int kBlk = 128;          // rows per tile (keys and queries)
 constexpr int kAtomBytes = 16384;  // 128 rows x 128 bytes
 constexpr int kThreads = 192;
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kHeadGroup = 16;  // heads scheduled together (their operands stay in L2)
 
 template <bool BF16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
@@ -187,8 +186,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                        const float* __restrict__ lse, const float* __restrict__ Drow,
-                       void* __restrict__ dk_out, void* __restrict__ dv_out, int heads, int Hq,
-                       int Hkv, int N, int causal, float scale, int* err) {
+                       void* __restrict__ dk_out, void* __restrict__ dv_out, int heads,
+                       int head_group, int Hq, int Hkv, int N, int causal, float scale, int* err) {
   using L = DkdvSmem<D>;
   constexpr int kAtoms = D / 64;
   extern __shared__ uint8_t smem_raw[];
@@ -202,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int T = (N + kBlk - 1) / kBlk;
   // Groups of KV heads whose Q and dO stay in L2; within a group the key tiles
   // with the most work under causal masking (small j) first.
-  const WorkItem wi = grouped_heavy_first(blockIdx.x, heads, T, kHeadGroup);
+  const WorkItem wi = grouped_heavy_first(blockIdx.x, heads, T, head_group);
   const int j = wi.rank;
   const int bkv = wi.head;  // b * Hkv + hkv
   const int b = bkv / Hkv;
@@ -502,8 +501,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                      const float* __restrict__ lse, const float* __restrict__ Drow,
-                     void* __restrict__ dq_out, int heads, int Hq, int Hkv, int N, int causal,
-                     float scale, int* err) {
+                     void* __restrict__ dq_out, int heads, int head_group, int Hq, int Hkv, int N,
+                     int causal, float scale, int* err) {
   using L = DqSmem<D>;
   constexpr int kAtoms = D / 64;
   extern __shared__ uint8_t smem_raw[];
@@ -517,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int T = (N + kBlk - 1) / kBlk;
   // Groups of query heads whose K and V stay in L2; within a group the query
   // tiles with the most key tiles under causal masking (large i) first.
-  const WorkItem wi = grouped_heavy_first(blockIdx.x, heads, T, kHeadGroup);
+  const WorkItem wi = grouped_heavy_first(blockIdx.x, heads, T, head_group);
   const int i = T - 1 - wi.rank;
   const int bhq = wi.head;  // b * Hq + hq
   const int b = bhq / Hq;
@@ -737,6 +736,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Heads scheduled side by side so that the operands they stream (per_head_bytes
+// each) stay within about a quarter of the 129 MB L2: 16 heads at N = 4096,
+// d = 128 (2 MB each), 4 at N = 16384.
+int l2_head_group(long per_head_bytes) {
+  long g = (32L << 20) / (per_head_bytes > 0 ? per_head_bytes : 1);
+  return static_cast<int>(g < 1 ? 1 : (g > 64 ? 64 : g));
+}
+
 int grid_for(long work_items, int per_block) {
   long blocks = (work_items + per_block - 1) / per_block;
   const long cap = 152L * 16;  // 16 resident 256-thread blocks per SM
@@ -766,13 +773,13 @@ cudaError_t launch_bwd_t(const AttnShape& s, const BwdArgs& a, cudaStream_t stre
 
   if (a.ev_before_dkdv && (e = cudaEventRecord(a.ev_before_dkdv, stream)) != cudaSuccess) return e;
   kdkdv<<<dim3(static_cast<unsigned>(T * s.B * s.Hkv)), kThreads, smem_kv, stream>>>(
-      a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.lse, a.D, a.dk, a.dv, s.B * s.Hkv, s.Hq, s.Hkv, s.N,
-      s.causal, s.scale, a.err);
+      a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.lse, a.D, a.dk, a.dv, s.B * s.Hkv,
+      l2_head_group(4L * s.N * D * (s.Hq / s.Hkv)), s.Hq, s.Hkv, s.N, s.causal, s.scale, a.err);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (a.ev_before_dq && (e = cudaEventRecord(a.ev_before_dq, stream)) != cudaSuccess) return e;
   kdq<<<dim3(static_cast<unsigned>(T * s.B * s.Hq)), kThreads, smem_q, stream>>>(
-      a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.lse, a.D, a.dq, s.B * s.Hq, s.Hq, s.Hkv, s.N, s.causal,
-      s.scale, a.err);
+      a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.lse, a.D, a.dq, s.B * s.Hq, l2_head_group(4L * s.N * D),
+      s.Hq, s.Hkv, s.N, s.causal, s.scale, a.err);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (a.ev_after_dq && (e = cudaEventRecord(a.ev_after_dq, stream)) != cudaSuccess) return e;
   return cudaSuccess;

@@ -46,7 +46,6 @@ constexpr int kThreads = 352;      // 11 warps
 // The two query tiles run half a period apart, so K_j is released by the
 // later tile; a third K stage lets K_{j+2} load while that tile finishes.
 constexpr int kKStages = 3;
-constexpr int kHeadGroup = 16;  // heads scheduled together (their K, V: 32 MB at N=4096)
 constexpr int kVStages = 2;
 
 template <int D>
@@ -97,8 +96,8 @@ template <int D, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, void* __restrict__ out,
-                  float* __restrict__ lse_out, int heads, int Hq, int Hkv, int N, int causal,
-                  float scale_log2, int* err) {
+                  float* __restrict__ lse_out, int heads, int head_group, int Hq, int Hkv, int N,
+                  int causal, float scale_log2, int* err) {
   using L = FwdSmem<D>;
   constexpr int kAtoms = D / 64;
   extern __shared__ uint8_t smem_raw[];
@@ -113,7 +112,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int T = (N + kBM - 1) / kBM;
   const int pairs = (T + 1) / 2;
   // Groups of heads whose K and V stay in L2; heaviest causal pairs first.
-  const WorkItem wi = grouped_heavy_first(blockIdx.x, heads, pairs, kHeadGroup);
+  const WorkItem wi = grouped_heavy_first(blockIdx.x, heads, pairs, head_group);
   const int pair = pairs - 1 - wi.rank;
   const int bh = wi.head;  // b * Hq + h
   const int h = bh % Hq;
@@ -421,8 +420,14 @@ cudaError_t launch_fwd_t(const AttnShape& s, const FwdArgs& a, cudaStream_t stre
   const int pairs = (T + 1) / 2;
   dim3 grid(static_cast<unsigned>(pairs * s.B * s.Hq));  // (head, pair) work items
   const float scale_log2 = s.scale * 1.4426950408889634f;
-  kern<<<grid, kThreads, smem, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.o, a.lse, s.B * s.Hq, s.Hq,
-                                         s.Hkv, s.N, s.causal, scale_log2, a.err);
+  // Heads side by side so that their K and V (4*N*d bytes per KV head, shared
+  // by Hq/Hkv query heads) stay within about a quarter of the L2.
+  const long kv_bytes_per_head = 4L * s.N * D / (s.Hq / s.Hkv);
+  long hg = (32L << 20) / (kv_bytes_per_head > 0 ? kv_bytes_per_head : 1);
+  hg = hg < 1 ? 1 : (hg > 64 ? 64 : hg);
+  kern<<<grid, kThreads, smem, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.o, a.lse, s.B * s.Hq,
+                                         static_cast<int>(hg), s.Hq, s.Hkv, s.N, s.causal,
+                                         scale_log2, a.err);
   return cudaGetLastError();
 }
 
