@@ -317,14 +317,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (c >= lim) x[c] = __float_as_uint(-INFINITY);
       }
       // row maximum as eight independent chains, then a tree
+      // eight chains (chain u: scores u, u+8, ..., u+120) of three-input maxima
       float m8[8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) m8[u] = __uint_as_float(x[u]);
+      for (int u = 0; u < 8; ++u) {
+        float m = fmax3(__uint_as_float(x[u]), __uint_as_float(x[u + 8]), __uint_as_float(x[u + 16]));
 #pragma unroll
-      for (int c = 8; c < kBN; ++c) m8[c & 7] = fmaxf(m8[c & 7], __uint_as_float(x[c]));
+        for (int k = 3; k < 15; k += 2)
+          m = fmax3(m, __uint_as_float(x[u + 8 * k]), __uint_as_float(x[u + 8 * k + 8]));
+        m8[u] = fmaxf(m, __uint_as_float(x[u + 120]));
+      }
       const float mx =
-          fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) *
-          sfac;
+          fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7])) * sfac;
       // Conditional rescale: keep the stale maximum unless it grew by more than 8
       // (p <= 2^8 then); the decision is warp-uniform because TMEM access is.
       float alpha = 1.0f;

@@ -345,6 +345,13 @@ __device__ __forceinline__ WorkItem grouped_heavy_first(int linear, int heads, i
 }
 
 // ---------------------------------------------------------------- math
+// Three-input maximum (one instruction on sm_100-class GPUs).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
