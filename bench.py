@@ -66,6 +66,25 @@ def flops_per_step():
     return f, b
 
 
+# ------------------------------------------------------------------ multi-rank
+def max_over_ranks(value: float, world: int, device) -> float:
+    """The largest `value` over all ranks (the job is as slow as its slowest replica)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_step: float, steps: int, world: int, max_ms: float) -> float:
+    """Every rank runs its own replica of the workload (weak scaling): the job
+    processes world * steps steps in the slowest rank's time."""
+    return world * flops_per_step * steps / (max_ms * 1e-3) / 1e12
+
+
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -309,18 +328,14 @@ def run_ours(args):
     clocks = sampler.stop()
     check_errors()
 
-    elapsed_ms = start.elapsed_time(end)
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(start.elapsed_time(end), world, dev)
     fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
     bwd_ms = statistics.mean(e[1].elapsed_time(e[5]) for e in evs)
     dkdv_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
     dq_ms = statistics.mean(e[3].elapsed_time(e[4]) for e in evs)
 
     f_fwd, f_bwd = flops_per_step()
-    value = world * (f_fwd + f_bwd) * K / (elapsed_ms * 1e-3) / 1e12
+    value = whole_job_tflops(f_fwd + f_bwd, K, world, elapsed_ms)
 
     # end-to-end through the public API with pinned host buffers: H2D of the
     # step's inputs, forward, backward, D2H of the gradients, every step.
@@ -350,13 +365,9 @@ def run_ours(args):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     check_errors()
-    e2e_value = world * (f_fwd + f_bwd) * E / (e2e_ms * 1e-3) / 1e12
+    e2e_value = whole_job_tflops(f_fwd + f_bwd, E, world, e2e_ms)
 
     if rank == 0:
         peaks, peak_kind = load_peaks()

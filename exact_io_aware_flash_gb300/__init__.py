@@ -9,4 +9,4 @@ in hand-written tcgen05/TMEM/TMA kernels behind the C ABI of ``libfa.so``
     dq, dk, dv = backward(q, k, v, o, lse, dO, causal=True)
 """
 from ._lib import (FAError, backward, check_errors, forward, load,  # noqa: F401
-                   set_backward_event_hooks, version, workspace_size)
+                   selftest_bounded_wait, set_backward_event_hooks, version, workspace_size)

@@ -54,6 +54,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.fa_backward_noalloc.restype = i
         lib.fa_set_backward_event_hooks.argtypes = [vp, vp, vp]
         lib.fa_set_backward_event_hooks.restype = i
+        lib.fa_selftest_bounded_wait.argtypes = [i, vp]
+        lib.fa_selftest_bounded_wait.restype = i
         lib.fa_check_errors.argtypes = [vp]
         lib.fa_check_errors.restype = i
         lib.fa_last_error.argtypes = []
@@ -167,6 +169,11 @@ def set_backward_event_hooks(before_dkdv=None, before_dq=None, after_dq=None) ->
     """
     evs = (before_dkdv, before_dq, after_dq)
     _raise(load().fa_set_backward_event_hooks(*(None if e is None else e.cuda_event for e in evs)))
+
+
+def selftest_bounded_wait(limit_ms: int = 50, stream=None) -> None:
+    """Enqueue a kernel whose bounded wait runs out (see fa.h); check_errors() then raises."""
+    _raise(load().fa_selftest_bounded_wait(int(limit_ms), _stream_handle(stream)))
 
 
 def check_errors(stream=None) -> None:

@@ -3,6 +3,7 @@
 // Host code only; the kernels live in fa_fwd.cu and fa_bwd.cu.
 #include "../../include/fa.h"
 #include "fa_internal.h"
+#include "ptx.cuh"
 
 #include <cmath>
 #include <cstdarg>
@@ -18,6 +19,20 @@ namespace {
 __device__ int g_fa_error_word;
 
 thread_local std::string t_last_error;
+
+// Self-test of the bounded waits: one thread waits on an mbarrier that nothing
+// ever completes; the wait gives up after limit_ns and raises the error word,
+// exactly as a stalled pipeline stage in the attention kernels would.
+__global__ void fa_selftest_wait_kernel(int* err, unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    fa::mbar_init(&bar, 1);
+    abort_flag = 0;
+    fa::fence_mbar_init();
+    (void)fa::mbar_wait_for(&bar, 0, &abort_flag, err, limit_ns);
+  }
+}
 thread_local cudaEvent_t t_ev_hooks[3] = {nullptr, nullptr, nullptr};
 
 int fail(int code, const char* fmt, ...) {
@@ -225,6 +240,19 @@ int fa_set_backward_event_hooks(void* before_dkdv, void* before_dq, void* after_
   t_ev_hooks[0] = static_cast<cudaEvent_t>(before_dkdv);
   t_ev_hooks[1] = static_cast<cudaEvent_t>(before_dq);
   t_ev_hooks[2] = static_cast<cudaEvent_t>(after_dq);
+  return FA_OK;
+}
+
+int fa_selftest_bounded_wait(int limit_ms, void* stream) {
+  t_last_error.clear();
+  if (limit_ms < 1 || limit_ms > 2000) return fail(FA_ERR_INVALID, "limit_ms must be in [1, 2000]");
+  DeviceState* st = nullptr;
+  int rc = get_device_state(&st);
+  if (rc) return rc;
+  fa_selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      st->err_word, static_cast<unsigned long long>(limit_ms) * 1000000ull);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(FA_ERR_CUDA, "self-test launch: %s", cudaGetErrorString(e));
   return FA_OK;
 }
 

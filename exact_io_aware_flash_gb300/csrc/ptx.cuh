@@ -79,8 +79,31 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Bounded wait for the phase of parity `parity` to complete.  Returns false if
-// the CTA-wide abort flag is raised or the limit expires (which raises both the
-// CTA flag and the global error word).  Never traps, never spins forever.
+// the CTA-wide abort flag is raised or `limit_ns` expires (which raises both
+// the CTA flag and the global error word).  Never traps, never spins forever.
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity,
+                                              volatile int* cta_abort, int* err_word,
+                                              unsigned long long limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  uint32_t spins = 0;
+  while (!mbar_try_wait(bar, parity)) {
+    if ((++spins & 63u) == 0) {
+      if (*cta_abort) return false;
+      if (*(volatile int*)err_word != kDevErrNone) {
+        *cta_abort = 1;
+        return false;
+      }
+      if (globaltimer_ns() - t0 > limit_ns) {
+        *cta_abort = 1;
+        atomicExch(err_word, kDevErrTimeout);
+        return false;
+      }
+    }
+  }
+  return true;
+}
+
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* cta_abort,
                                           int* err_word) {
   if (mbar_try_wait(bar, parity)) return true;

@@ -168,6 +168,17 @@ FA_API int fa_set_backward_event_hooks(void* before_dkdv, void* before_dq, void*
  */
 FA_API int fa_check_errors(void* stream);
 
+/*
+ * Self-test of the failure detection.  Enqueues on `stream` a one-thread
+ * kernel that waits on an mbarrier nothing ever completes, using the same
+ * bounded wait as the attention kernels but with a limit of `limit_ms`
+ * milliseconds (1..2000).  When the limit expires the kernel raises the device
+ * error word and returns normally, so a following fa_check_errors(stream)
+ * reports FA_ERR_TIMEOUT (and clears the word) while the CUDA context stays
+ * usable.  Returns FA_OK once enqueued, FA_ERR_INVALID for a bad limit.
+ */
+FA_API int fa_selftest_bounded_wait(int limit_ms, void* stream);
+
 /* Message for the last error returned on the calling host thread ("" if none). */
 FA_API const char* fa_last_error(void);
 
