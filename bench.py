@@ -443,13 +443,25 @@ def sweep(dev):
                                                   make_inputs)
 
     def timed(fn, iters=20):
+        """Device time per call: `iters` calls captured in a CUDA graph and replayed,
+        so host-side launch cost does not enter small cases."""
         for _ in range(3):
             fn()
         torch.cuda.synchronize()
+        check_errors()
+        graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(graph, stream=side):
+                for _ in range(iters):
+                    fn()
+        torch.cuda.current_stream().wait_stream(side)
+        graph.replay()
+        torch.cuda.synchronize()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
-        for _ in range(iters):
-            fn()
+        graph.replay()
         b.record()
         torch.cuda.synchronize()
         check_errors()

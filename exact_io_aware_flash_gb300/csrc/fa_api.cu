@@ -9,6 +9,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 #include <string>
 
@@ -144,6 +145,20 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 }  // namespace
 
 namespace fa {
+
+cudaError_t set_smem_once(const void* kernel, int bytes, int slot) {
+  // slot: a small per-kernel index; one flag per (device, slot)
+  static std::atomic<int> done[kMaxDevices][32];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices || slot < 0 || slot >= 32)
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (done[dev][slot].load(std::memory_order_acquire)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done[dev][slot].store(1, std::memory_order_release);
+  return e;
+}
 
 int set_last_error(int code, const char* fmt, ...) {
   char buf[512];

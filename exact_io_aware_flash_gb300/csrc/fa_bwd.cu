@@ -762,13 +762,12 @@ cudaError_t launch_bwd_t(const AttnShape& s, const BwdArgs& a, cudaStream_t stre
   const int T = (s.N + kBlk - 1) / kBlk;
   auto kdkdv = fa_bwd_dkdv_kernel<D, BF16>;
   constexpr int smem_kv = DkdvSmem<D>::kAlloc;
-  if ((e = cudaFuncSetAttribute(kdkdv, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_kv)) !=
-      cudaSuccess)
+  const int slot = (D == 64 ? 0 : 2) + (BF16 ? 1 : 0);
+  if ((e = set_smem_once(reinterpret_cast<const void*>(kdkdv), smem_kv, 8 + slot)) != cudaSuccess)
     return e;
   auto kdq = fa_bwd_dq_kernel<D, BF16>;
   constexpr int smem_q = DqSmem<D>::kAlloc;
-  if ((e = cudaFuncSetAttribute(kdq, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_q)) !=
-      cudaSuccess)
+  if ((e = set_smem_once(reinterpret_cast<const void*>(kdq), smem_q, 16 + slot)) != cudaSuccess)
     return e;
 
   if (a.ev_before_dkdv && (e = cudaEventRecord(a.ev_before_dkdv, stream)) != cudaSuccess) return e;

@@ -418,7 +418,8 @@ template <int D, bool BF16>
 cudaError_t launch_fwd_t(const AttnShape& s, const FwdArgs& a, cudaStream_t stream) {
   auto kern = fa_fwd_kernel<D, BF16>;
   constexpr int smem = FwdSmem<D>::kAlloc;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), smem,
+                                (D == 64 ? 0 : 2) + (BF16 ? 1 : 0));
   if (e != cudaSuccess) return e;
   const int T = (s.N + kBM - 1) / kBM;
   const int pairs = (T + 1) / 2;

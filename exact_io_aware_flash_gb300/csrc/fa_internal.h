@@ -45,6 +45,10 @@ struct BwdArgs {
 cudaError_t launch_forward(const AttnShape& s, const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_backward(const AttnShape& s, const BwdArgs& a, cudaStream_t stream);
 
+// Raises a kernel's dynamic shared-memory limit to `bytes` once per device
+// (cudaFuncSetAttribute is a host round trip; calls after the first are free).
+cudaError_t set_smem_once(const void* kernel, int bytes, int slot);
+
 // Records `fmt` as the calling thread's fa_last_error() message; returns `code`.
 int set_last_error(int code, const char* fmt, ...);
 
