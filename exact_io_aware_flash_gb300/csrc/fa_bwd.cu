@@ -160,8 +160,8 @@ struct DkdvSmem {
   static constexpr int kV = kK + kTile;
   static constexpr int kQ = kV + kTile;        // 2 stages
   static constexpr int kdO = kQ + 2 * kTile;   // 2 stages
-  static constexpr int kLse = kdO + 2 * kTile; // 2 stages x 128 floats: LSE * log2(e)
-  static constexpr int kDrow = kLse + 1024;    // 2 stages x 128 floats: D
+  static constexpr int kLse = kdO + 2 * kTile; // 2 stages x 128 floats: -LSE * log2(e)
+  static constexpr int kDrow = kLse + 1024;    // 2 stages x 128 floats: -D
   static constexpr int kBar = kDrow + 1024;
   static constexpr int kBytes = kBar + 256;
   static constexpr int kAlloc = kBytes + 1024;
@@ -269,16 +269,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) == 0) break;  // also orders the stage reuse
-      // LSE (as log2) and D of the tile's 128 query rows; padding rows get
-      // LSE = +inf so their recomputed probabilities are exactly 0.
+      // -LSE (as log2) and -D of the tile's 128 query rows, negated so the
+      // compute warps add them; padding rows get LSE = +inf so their recomputed
+      // probabilities are exactly 0.
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int r = lane * 4 + e;
         const int qrow = i * kBlk + r;
         const size_t g = static_cast<size_t>(bhq) * N + qrow;
         const bool in = qrow < N;
-        s_lse[st * 128 + r] = in ? lse[g] * kLog2e : INFINITY;
-        s_d[st * 128 + r] = in ? Drow[g] : 0.f;
+        s_lse[st * 128 + r] = in ? -lse[g] * kLog2e : -INFINITY;
+        s_d[st * 128 + r] = in ? -Drow[g] : 0.f;
       }
       mbar_arrive(&bar[KB_QFULL + st]);
     }
@@ -366,6 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tmem + lane_off + kColS;
     const uint32_t tP = tmem + lane_off + kColDP;
     const float sl2 = scale * kLog2e;
+    const uint64_t sl2x2 = f2_pack(sl2, sl2);
     const float* s_lse = reinterpret_cast<const float*>(smem + L::kLse);
     const float* s_d = reinterpret_cast<const float*>(smem + L::kDrow);
     bool ok = true;
@@ -390,11 +392,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         reg_fence<64>(sv);
 #pragma unroll
         for (int c = 0; c < 64; c += 4) {
-          const float4 l4 = lds128_ordered(lse2 + h + c);
-          p[h + c] = ex2_approx(fmaf(__uint_as_float(sv[c]), sl2, -l4.x));
-          p[h + c + 1] = ex2_approx(fmaf(__uint_as_float(sv[c + 1]), sl2, -l4.y));
-          p[h + c + 2] = ex2_approx(fmaf(__uint_as_float(sv[c + 2]), sl2, -l4.z));
-          p[h + c + 3] = ex2_approx(fmaf(__uint_as_float(sv[c + 3]), sl2, -l4.w));
+          const float4 l4 = lds128_ordered(lse2 + h + c);  // -LSE_q * log2(e)
+          float a0, a1, a2, a3;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sl2x2,
+                           f2_pack(l4.x, l4.y)),
+                    a0, a1);
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3])), sl2x2,
+                           f2_pack(l4.z, l4.w)),
+                    a2, a3);
+          p[h + c] = ex2_approx(a0);
+          p[h + c + 1] = ex2_approx(a1);
+          p[h + c + 2] = ex2_approx(a2);
+          p[h + c + 3] = ex2_approx(a3);
         }
       }
       if (diag) {
@@ -427,11 +436,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
-          const float4 d4 = lds128_ordered(dd + c + e);
-          pk[e / 2] = pack2<BF16>(p[c + e] * (__uint_as_float(dpv[e]) - d4.x),
-                                  p[c + e + 1] * (__uint_as_float(dpv[e + 1]) - d4.y));
-          pk[e / 2 + 1] = pack2<BF16>(p[c + e + 2] * (__uint_as_float(dpv[e + 2]) - d4.z),
-                                      p[c + e + 3] * (__uint_as_float(dpv[e + 3]) - d4.w));
+          const float4 d4 = lds128_ordered(dd + c + e);  // -D_q
+          float g0, g1, g2, g3;
+          f2_unpack(f2_mul(f2_pack(p[c + e], p[c + e + 1]),
+                           f2_add(f2_pack(__uint_as_float(dpv[e]), __uint_as_float(dpv[e + 1])),
+                                  f2_pack(d4.x, d4.y))),
+                    g0, g1);
+          f2_unpack(f2_mul(f2_pack(p[c + e + 2], p[c + e + 3]),
+                           f2_add(f2_pack(__uint_as_float(dpv[e + 2]), __uint_as_float(dpv[e + 3])),
+                                  f2_pack(d4.z, d4.w))),
+                    g2, g3);
+          pk[e / 2] = pack2<BF16>(g0, g1);
+          pk[e / 2 + 1] = pack2<BF16>(g2, g3);
         }
         tmem_st16(tP + c / 2, pk);
       }
@@ -663,6 +679,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Padding rows (q >= N) get LSE = +inf: P and dS are exactly 0 there.
     const float lse2 = (q < N) ? lse[g] * kLog2e : INFINITY;
     const float dq_d = (q < N) ? Drow[g] : 0.f;
+    const uint64_t negd2 = f2_pack(-dq_d, -dq_d);
     bool ok = true;
     for (int jj = 0; jj < n_j; ++jj) {
       ok = __all_sync(0xffffffffu, mbar_wait(&bar[QB_SFULL], jj & 1, abort_flag, err));
@@ -678,8 +695,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar[QB_SFREE]);
+        const uint64_t sl2x2 = f2_pack(sl2, sl2);
+        const uint64_t nl2 = f2_pack(-lse2, -lse2);
 #pragma unroll
-        for (int c = 0; c < kBlk; ++c) p[c] = ex2_approx(fmaf(__uint_as_float(sv[c]), sl2, -lse2));
+        for (int c = 0; c < kBlk; c += 2) {
+          float a0, a1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sl2x2, nl2),
+                    a0, a1);
+          p[c] = ex2_approx(a0);
+          p[c + 1] = ex2_approx(a1);
+        }
       }
       if (causal && jj == i) {  // key j*128 + c after query i*128 + t is masked
 #pragma unroll
@@ -708,9 +733,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 64; c += 32) {
           uint32_t dsw[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            dsw[e] = pack2<BF16>(p[h + c + 2 * e] * (__uint_as_float(dpv[c + 2 * e]) - dq_d),
-                                 p[h + c + 2 * e + 1] * (__uint_as_float(dpv[c + 2 * e + 1]) - dq_d));
+          for (int e = 0; e < 16; ++e) {
+            float g0, g1;
+            f2_unpack(f2_mul(f2_pack(p[h + c + 2 * e], p[h + c + 2 * e + 1]),
+                             f2_add(f2_pack(__uint_as_float(dpv[c + 2 * e]),
+                                            __uint_as_float(dpv[c + 2 * e + 1])),
+                                    negd2)),
+                      g0, g1);
+            dsw[e] = pack2<BF16>(g0, g1);
+          }
           tmem_st16(tDS + (h + c) / 2, dsw);
         }
       }

@@ -343,21 +343,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_run = mx;
         }
       }
-      float rs[4] = {0.f, 0.f, 0.f, 0.f};
-      const float neg_m = -m_run;
+      // exponent arguments and row sums two at a time (packed fp32)
+      const uint64_t sfac2 = f2_pack(sfac, sfac);
+      const uint64_t negm2 = f2_pack(-m_run, -m_run);
+      uint64_t rs2[2] = {0ull, 0ull};
 #pragma unroll
       for (int c = 0; c < kBN; c += 32) {
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float p0 = ex2_approx(fmaf(__uint_as_float(x[c + 2 * e]), sfac, neg_m));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(x[c + 2 * e + 1]), sfac, neg_m));
-          rs[e & 3] += p0 + p1;
+          float a0, a1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(x[c + 2 * e]), __uint_as_float(x[c + 2 * e + 1])),
+                           sfac2, negm2),
+                    a0, a1);
+          const float p0 = ex2_approx(a0);
+          const float p1 = ex2_approx(a1);
+          rs2[e & 1] = f2_add(rs2[e & 1], f2_pack(p0, p1));
           pk[e] = pack2<BF16>(p0, p1);
         }
         tmem_st16(tS + c / 2, pk);
       }
-      l_run = l_run * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
+      float r0, r1, r2, r3;
+      f2_unpack(rs2[0], r0, r1);
+      f2_unpack(rs2[1], r2, r3);
+      l_run = l_run * alpha + ((r0 + r1) + (r2 + r3));
       if (rescale) {
         // O_X was last written by PV_X(j-1), which completed before S_X(j) was issued.
 #pragma unroll
