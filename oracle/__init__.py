@@ -70,6 +70,8 @@ class Oracle:
         lib.oracle_backward.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp,
                                         i, i, i, i, i, i, ctypes.c_double]
         lib.oracle_backward.restype = i
+        lib.oracle_forward_rect.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, i, i, ctypes.c_double]
+        lib.oracle_forward_rect.restype = i
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = i
         self.lib = lib
@@ -93,6 +95,20 @@ class Oracle:
                                      B, Hq, Hkv, N, d, int(bool(causal)), float(scale))
         if rc != 0:
             raise ValueError(f"oracle_forward failed with code {rc}")
+        return o, lse
+
+    def forward_rect(self, q, k, v, scale: float):
+        """Non-causal forward with Nq query rows and Nk keys: q [B,Hq,Nq,d], k, v [B,Hkv,Nk,d]."""
+        q, k, v = _as_f64(q), _as_f64(k), _as_f64(v)
+        B, Hq, Nq, d = q.shape
+        Hkv, Nk = k.shape[1], k.shape[2]
+        assert k.shape == (B, Hkv, Nk, d) and v.shape == k.shape
+        o = np.empty_like(q)
+        lse = np.empty((B, Hq, Nq), dtype=np.float64)
+        rc = self.lib.oracle_forward_rect(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                          B, Hq, Hkv, Nq, Nk, d, float(scale))
+        if rc != 0:
+            raise ValueError(f"oracle_forward_rect failed with code {rc}")
         return o, lse
 
     def backward(self, q, k, v, dO, causal: bool, scale: float):
@@ -136,3 +152,8 @@ def forward(q, k, v, causal: bool, scale: float):
 def backward(q, k, v, dO, causal: bool, scale: float):
     """See ``Oracle.backward``."""
     return _default().backward(q, k, v, dO, causal, scale)
+
+
+def forward_rect(q, k, v, scale: float):
+    """See ``Oracle.forward_rect``."""
+    return _default().forward_rect(q, k, v, scale)

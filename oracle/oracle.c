@@ -142,6 +142,49 @@ int oracle_forward(const double* q, const double* k, const double* v, double* o,
 }
 
 /*
+ * Forward with Nq query rows and Nk keys per head (non-causal): the same
+ * definition with a rectangular score matrix, as used for decoding, where a
+ * few new query rows attend to a long sequence of cached keys.
+ *   q, o : [B, Hq, Nq, d]    k, v : [B, Hkv, Nk, d]    lse : [B, Hq, Nq]
+ */
+int oracle_forward_rect(const double* q, const double* k, const double* v, double* o,
+                        double* lse, int B, int Hq, int Hkv, int Nq, int Nk, int d,
+                        double scale) {
+    int rc = check_args(B, Hq, Hkv, Nq, d);
+    if (rc) return rc;
+    if (Nk <= 0) return ORACLE_EINVAL;
+    if (!q || !k || !v || !o || !lse) return ORACLE_EINVAL;
+    const int64_t rows = (int64_t)B * Hq * Nq;
+    int failed = 0;
+#pragma omp parallel
+    {
+        double* p = (double*)malloc(sizeof(double) * (size_t)Nk);
+        if (!p) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(dynamic, 4)
+        for (int64_t r = 0; r < rows; ++r) {
+            if (!p) continue;
+            const int64_t bh = r / Nq;
+            const int h = (int)(bh % Hq);
+            const int b = (int)(bh / Hq);
+            const int g = (int)(((int64_t)h * Hkv) / Hq);
+            const double* qi = q + (size_t)r * d;
+            const double* kh = k + ((size_t)b * Hkv + g) * (size_t)Nk * d;
+            const double* vh = v + ((size_t)b * Hkv + g) * (size_t)Nk * d;
+            lse[r] = softmax_row(qi, kh, Nk, d, scale, p);
+            double* oi = o + (size_t)r * d;
+            for (int c = 0; c < d; ++c) oi[c] = 0.0;
+            for (int kk = 0; kk < Nk; ++kk)
+                for (int c = 0; c < d; ++c) oi[c] += p[kk] * vh[(size_t)kk * d + c];
+        }
+        free(p);
+    }
+    return failed ? ORACLE_ENOMEM : ORACLE_OK;
+}
+
+/*
  * Backward from the definition.  Recomputes P and O itself from (q, k, v); it
  * takes no forward output from anywhere else.  D (may be NULL) receives
  * D_i = dO_i . O_i.  KV heads are processed one after another; within one, the

@@ -27,8 +27,13 @@ MUTATIONS = [
      "const int nk = causal ? i : N;\n            lse"),
     ("lse_without_max", "return m + log(l);", "return log(l);"),
     ("no_max_shift", "p[k] = exp(p[k] - m);", "p[k] = exp(p[k]);"),
-    ("gqa_modulo_map", "const int g = (int)(((int64_t)h * Hkv) / Hq);",
-     "const int g = (int)(h % Hkv);"),
+    ("gqa_modulo_map",
+     "const int g = (int)(((int64_t)h * Hkv) / Hq);\n            const double* qi = q + (size_t)r * d;\n"
+     "            const double* kh = k + ((size_t)b * Hkv + g) * (size_t)N * d;",
+     "const int g = (int)(h % Hkv);\n            const double* qi = q + (size_t)r * d;\n"
+     "            const double* kh = k + ((size_t)b * Hkv + g) * (size_t)N * d;"),
+    ("rect_drops_last_key", "lse[r] = softmax_row(qi, kh, Nk, d, scale, p);",
+     "lse[r] = softmax_row(qi, kh, Nk - 1, d, scale, p);"),
     ("unnormalised_p", "for (int k = 0; k < nk; ++k) p[k] /= l;", ""),
     ("transposed_dq_operand", "dqi[c] += ds[kk] * kh[(size_t)kk * d + c];",
      "dqi[c] += ds[kk] * vh[(size_t)kk * d + c];"),
@@ -69,6 +74,13 @@ def _checks_fail(o: "oracle.Oracle") -> bool:
         for a, b in zip((dq, dk, dv), ref[:3]):
             if not np.allclose(a, b, atol=1e-9):
                 return True
+    # rectangular (decoding) forward: 3 query rows against 9 keys
+    qr, kr, vr = rng.standard_normal((B, Hq, 3, d)), rng.standard_normal((B, Hkv, 9, d)), \
+        rng.standard_normal((B, Hkv, 9, d))
+    o_r, l_r = o.forward_rect(qr, kr, vr, s)
+    o_n, l_n, _ = naive.forward(qr, kr, vr, False, s)
+    if not (np.allclose(o_r, o_n, atol=1e-9) and np.allclose(l_r, l_n, atol=1e-9)):
+        return True
     return False
 
 

@@ -228,3 +228,33 @@ def test_online_recurrence_reproduces_definition(form, causal):
 def test_rejects_bad_head_grouping():
     with pytest.raises(ValueError):
         oracle.forward(rand(1, 3, 4, 2), rand(1, 2, 4, 2), rand(1, 2, 4, 2), False, 1.0)
+
+
+# ---------------------------------------------------------------- rectangular (decoding) forward
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk,d", [(1, 1, 1, 1, 1, 4), (2, 4, 2, 1, 13, 8),
+                                              (1, 3, 1, 5, 40, 4), (1, 2, 2, 17, 3, 8)])
+def test_rect_forward_bruteforce(B, Hq, Hkv, Nq, Nk, d):
+    q, k, v = rand(B, Hq, Nq, d), rand(B, Hkv, Nk, d), rand(B, Hkv, Nk, d)
+    o, lse = oracle.forward_rect(q, k, v, 0.7)
+    o_n, lse_n, _ = naive.forward(q, k, v, False, 0.7)
+    np.testing.assert_allclose(o, o_n, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, lse_n, rtol=0, atol=1e-12)
+
+
+def test_rect_forward_closed_forms_and_square_case():
+    # identical keys: O = mean(V), LSE = s q.k + ln Nk; one key: O = V_0
+    Nq, Nk, d, s = 3, 11, 5, 0.4
+    q, v = rand(1, 1, Nq, d), rand(1, 1, Nk, d)
+    krow = rand(d)
+    k = np.broadcast_to(krow, (1, 1, Nk, d)).copy()
+    o, lse = oracle.forward_rect(q, k, v, s)
+    np.testing.assert_allclose(o[0, 0], np.broadcast_to(v[0, 0].mean(0), (Nq, d)), atol=1e-12)
+    np.testing.assert_allclose(lse[0, 0], s * (q[0, 0] @ krow) + np.log(Nk), atol=1e-12)
+    o1, _ = oracle.forward_rect(q, k[:, :, :1], v[:, :, :1], s)
+    np.testing.assert_allclose(o1[0, 0], np.broadcast_to(v[0, 0, 0], (Nq, d)), atol=1e-15)
+    # Nq = Nk agrees with the square non-causal forward
+    qs, ks, vs = rand(1, 2, 9, 4), rand(1, 2, 9, 4), rand(1, 2, 9, 4)
+    a, la = oracle.forward_rect(qs, ks, vs, 0.5)
+    b, lb = oracle.forward(qs, ks, vs, False, 0.5)
+    np.testing.assert_allclose(a, b, atol=1e-14)
+    np.testing.assert_allclose(la, lb, atol=1e-14)
