@@ -437,7 +437,8 @@ def sweep(dev):
     """Extra lines (not the bench line): forward workloads and the backward sweep."""
     import torch
 
-    from exact_io_aware_flash_gb300 import backward, check_errors, forward, workspace_size
+    from exact_io_aware_flash_gb300 import (backward, check_errors, forward, forward_splitkv,
+                                            workspace_size)
     from exact_io_aware_flash_gb300.flops import backward_flops, forward_flops
     from exact_io_aware_flash_gb300.synth import (BACKWARD_SWEEP_N, WORKLOADS, backward_sweep_shape,
                                                   make_inputs)
@@ -476,6 +477,17 @@ def sweep(dev):
             fl = forward_flops(s.B, s.Hq, s.N, s.d, causal)
             print(json.dumps({"sweep": "forward", "workload": name, "causal": causal, "ms": ms,
                               "tflops": fl / ms / 1e9}), flush=True)
+    # decoding: one new query row per head against a 32k-token cache (GQA 32/8)
+    B, Hq, Hkv, Nk, d = 8, 32, 8, 32768, 128
+    qd = torch.randn(B, Hq, 1, d, device=dev, dtype=torch.bfloat16)
+    kd = torch.randn(B, Hkv, Nk, d, device=dev, dtype=torch.bfloat16)
+    vd = torch.randn_like(kd)
+    ms = timed(lambda: forward_splitkv(qd, kd, vd))
+    kv_bytes = 2 * kd.numel() * kd.element_size()
+    peaks, _ = load_peaks()
+    print(json.dumps({"sweep": "decode", "B": B, "Hq": Hq, "Hkv": Hkv, "Nq": 1, "Nk": Nk, "d": d,
+                      "ms": ms, "kv_gbs": kv_bytes / ms / 1e6,
+                      "frac_of_hbm": kv_bytes / ms / 1e6 / peaks["hbm_gbs"]}), flush=True)
     for N in BACKWARD_SWEEP_N:
         s = backward_sweep_shape(N)
         inp = make_inputs(s, "bf16", seed=1005 + N)

@@ -50,6 +50,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.fa_backward_workspace_size.restype = sz
         lib.fa_backward.argtypes = [vp] * 10 + [sz] + [i] * 6 + [f, i, vp]
         lib.fa_backward.restype = i
+        lib.fa_forward_splitkv_workspace_size.argtypes = [i] * 7
+        lib.fa_forward_splitkv_workspace_size.restype = sz
+        lib.fa_forward_splitkv.argtypes = [vp] * 5 + [i] * 6 + [f, i, i, vp, sz, vp]
+        lib.fa_forward_splitkv.restype = i
         lib.fa_backward_noalloc.argtypes = [vp] * 9 + [i] * 6 + [f, i, vp]
         lib.fa_backward_noalloc.restype = i
         lib.fa_set_backward_event_hooks.argtypes = [vp, vp, vp]
@@ -127,6 +131,37 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None,
     rc = load().fa_forward(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                            lse.data_ptr(), B, Hq, Hkv, N, d, int(bool(causal)), float(scale),
                            _dtype_code(q), _stream_handle(stream))
+    _raise(rc)
+    return out, lse
+
+
+def forward_splitkv(q, k, v, scale: float | None = None, num_splits: int = 0, out=None, lse=None,
+                    workspace=None, stream=None):
+    """Split-KV (decoding) forward: q [B, Hq, Nq, d] against k, v [B, Hkv, Nk, d], non-causal.
+
+    Returns (o [B,Hq,Nq,d], lse [B,Hq,Nq] float32).  num_splits <= 0 lets the
+    library choose the number of key chunks.
+    """
+    B, Hq, Nq, d = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    _check(q, "q", (B, Hq, Nq, d), q.dtype)
+    _check(k, "k", (B, Hkv, Nk, d), q.dtype)
+    _check(v, "v", (B, Hkv, Nk, d), q.dtype)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check(out, "out", (B, Hq, Nq, d), q.dtype)
+    _check(lse, "lse", (B, Hq, Nq), torch.float32)
+    lib = load()
+    ws_bytes = int(lib.fa_forward_splitkv_workspace_size(B, Hq, Hkv, Nq, Nk, d, int(num_splits)))
+    if workspace is None and ws_bytes:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_len = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = lib.fa_forward_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                lse.data_ptr(), B, Hq, Hkv, Nq, Nk, d, float(scale), _dtype_code(q),
+                                int(num_splits), ws_ptr, ws_len, _stream_handle(stream))
     _raise(rc)
     return out, lse
 

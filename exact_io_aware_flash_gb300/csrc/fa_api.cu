@@ -146,6 +146,19 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 namespace fa {
 
+int sm_count() {
+  static std::atomic<int> cached[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+  int n = cached[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    cached[dev].store(n, std::memory_order_relaxed);
+  }
+  return n;
+}
+
 cudaError_t set_smem_once(const void* kernel, int bytes, int slot) {
   // slot: a small per-kernel index; one flag per (device, slot)
   static std::atomic<int> done[kMaxDevices][32];
@@ -198,6 +211,94 @@ int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse,
   a.err = st->err_word;
   cudaError_t e = fa::launch_forward(s, a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(FA_ERR_CUDA, "forward launch: %s", cudaGetErrorString(e));
+  return FA_OK;
+}
+
+namespace {
+
+struct SplitPlan {
+  int splits, chunk_tiles;
+};
+
+// Key chunks for the split-KV forward: enough CTAs for about two waves of the
+// device's SMs, at least one 128-key tile per chunk, no empty chunk.
+SplitPlan plan_splits(int B, int Hq, int Hkv, int Nq, int Nk, int requested) {
+  const long Mq = static_cast<long>(Hq / Hkv) * Nq;
+  const long base = ((Mq + 127) / 128) * B * Hkv;
+  const int KT = (Nk + 127) / 128;
+  long want = requested;
+  if (want <= 0) {
+    int sms = 148;
+    int dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess) sms = fa::sm_count();
+    want = (2L * sms + base - 1) / base;
+  }
+  if (want < 1) want = 1;
+  if (want > KT) want = KT;
+  const int chunk = static_cast<int>((KT + want - 1) / want);
+  return SplitPlan{(KT + chunk - 1) / chunk, chunk};
+}
+
+size_t splitkv_ws_bytes(int B, int Hq, int Nq, int d, int splits) {
+  if (splits <= 1) return 0;
+  const size_t rows = static_cast<size_t>(B) * Hq * Nq;
+  return round_up(static_cast<size_t>(splits) * rows * d * 4, 256) +
+         round_up(static_cast<size_t>(splits) * rows * 4, 256);
+}
+
+}  // namespace
+
+size_t fa_forward_splitkv_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int d,
+                                         int num_splits) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nq <= 0 || Nk <= 0 || d <= 0 || Hq % Hkv) return 0;
+  return splitkv_ws_bytes(B, Hq, Nq, d, plan_splits(B, Hq, Hkv, Nq, Nk, num_splits).splits);
+}
+
+int fa_forward_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                       int Hq, int Hkv, int Nq, int Nk, int d, float scale, int dtype,
+                       int num_splits, void* workspace, size_t ws_bytes, void* stream) {
+  t_last_error.clear();
+  if (!q || !k || !v || !o || !lse) return fail(FA_ERR_INVALID, "null tensor pointer");
+  if (Nk <= 0) return fail(FA_ERR_INVALID, "Nk must be positive");
+  int rc = check_common(B, Hq, Hkv, Nq, d, scale, dtype);
+  if (rc) return rc;
+  if ((long long)B * Hkv * Nk > 0x7fffffffLL) return fail(FA_ERR_UNSUPPORTED, "B*Hkv*Nk exceeds 2^31-1");
+  const void* ptrs[] = {q, k, v, o, lse};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return fail(FA_ERR_UNSUPPORTED, "all tensor pointers must be 16-byte aligned");
+  DeviceState* st = nullptr;
+  if ((rc = get_device_state(&st))) return rc;
+  const SplitPlan plan = plan_splits(B, Hq, Hkv, Nq, Nk, num_splits);
+  const size_t need = splitkv_ws_bytes(B, Hq, Nq, d, plan.splits);
+  if (need > 0) {
+    if (!workspace || ws_bytes < need)
+      return fail(FA_ERR_INVALID, "split-KV workspace of %zu bytes is smaller than the %zu required",
+                  workspace ? ws_bytes : (size_t)0, need);
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+      return fail(FA_ERR_UNSUPPORTED, "workspace must be 256-byte aligned");
+  }
+  const long grid = ((static_cast<long>(Hq / Hkv) * Nq + 127) / 128) * B * Hkv * plan.splits;
+  if (grid > 0x7fffffffL) return fail(FA_ERR_UNSUPPORTED, "problem too large for one launch");
+  fa::AttnShape s{B, Hq, Hkv, Nq, d, 0, scale, dtype == FA_DTYPE_BF16};
+  fa::DecodeArgs a{};
+  const int Mq = (Hq / Hkv) * Nq;
+  if ((rc = encode_tile_map(&a.tm_q, q, B * Hkv, Mq, d, s.bf16, "q"))) return rc;
+  if ((rc = encode_tile_map(&a.tm_k, k, B * Hkv, Nk, d, s.bf16, "k"))) return rc;
+  if ((rc = encode_tile_map(&a.tm_v, v, B * Hkv, Nk, d, s.bf16, "v"))) return rc;
+  a.o = o;
+  a.lse = lse;
+  const size_t rows = static_cast<size_t>(B) * Hq * Nq;
+  a.o_part = static_cast<float*>(workspace);
+  a.lse_part = need ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                               round_up(static_cast<size_t>(plan.splits) * rows * d * 4, 256))
+                    : nullptr;
+  a.Nq = Nq;
+  a.Nk = Nk;
+  a.splits = plan.splits;
+  a.chunk_tiles = plan.chunk_tiles;
+  a.err = st->err_word;
+  cudaError_t e = fa::launch_decode(s, a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(FA_ERR_CUDA, "split-KV forward launch: %s", cudaGetErrorString(e));
   return FA_OK;
 }
 

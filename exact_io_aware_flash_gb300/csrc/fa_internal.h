@@ -41,13 +41,28 @@ struct BwdArgs {
   cudaEvent_t ev_after_dq;
 };
 
+// Split-KV forward (decoding): q [B, Hq, Nq, d] seen as [B*Hkv, (Hq/Hkv)*Nq, d].
+struct DecodeArgs {
+  CUtensorMap tm_q, tm_k, tm_v;
+  void* o;
+  float* lse;
+  float* o_part;    // [splits][B*Hq*Nq][d] fp32 (splits > 1)
+  float* lse_part;  // [splits][B*Hq*Nq]
+  int Nq, Nk, splits, chunk_tiles;
+  int* err;
+};
+
 // Each returns cudaSuccess or the launch error.  `stream` is the caller's.
 cudaError_t launch_forward(const AttnShape& s, const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_backward(const AttnShape& s, const BwdArgs& a, cudaStream_t stream);
+cudaError_t launch_decode(const AttnShape& s, const DecodeArgs& a, cudaStream_t stream);
 
 // Raises a kernel's dynamic shared-memory limit to `bytes` once per device
 // (cudaFuncSetAttribute is a host round trip; calls after the first are free).
 cudaError_t set_smem_once(const void* kernel, int bytes, int slot);
+
+// Streaming multiprocessors of the current device (cached per device).
+int sm_count();
 
 // Records `fmt` as the calling thread's fa_last_error() message; returns `code`.
 int set_last_error(int code, const char* fmt, ...);
@@ -55,5 +70,6 @@ int set_last_error(int code, const char* fmt, ...);
 // Shared-memory bytes the forward kernel needs for head dimension d (for checks).
 size_t forward_smem_bytes(int d);
 size_t backward_smem_bytes(int d);
+size_t decode_smem_bytes(int d);
 
 }  // namespace fa

@@ -84,6 +84,31 @@ FA_API int fa_forward(const void* q, const void* k, const void* v, void* o, floa
                int Hkv, int N, int d, int causal, float scale, int dtype, void* stream);
 
 /*
+ * Split-KV forward for decoding: a few query rows against a long key sequence
+ * ("Flash Attention" (aiwiki.ai), section "Flash-Decoding": split the keys
+ * into chunks, attend to each chunk with its own log-sum-exp, combine).
+ *
+ *   q, o : [B, Hq, Nq, d]    k, v : [B, Hkv, Nk, d]    lse : [B, Hq, Nq] fp32
+ *
+ * Non-causal: every query row attends to all Nk keys (a decoding step's new
+ * tokens against the full cache).  O and LSE have the same meaning as in
+ * fa_forward.  The query rows of the Hq/Hkv heads that share a KV head are
+ * processed together, so each key/value tile is read once per KV head.
+ *
+ * num_splits: number of key chunks; <= 0 chooses one from the problem size and
+ * the device's SM count; it is clamped to the number of 128-key tiles.  With
+ * more than one split the partial results go through `workspace` (device
+ * memory, 256-byte aligned, at least fa_forward_splitkv_workspace_size() bytes
+ * for the same arguments; may be NULL when that size is 0).  Nq, Nk >= 1.
+ * Same conventions, errors and asynchrony as fa_forward otherwise.
+ */
+FA_API size_t fa_forward_splitkv_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int d,
+                                                int num_splits);
+FA_API int fa_forward_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                              int B, int Hq, int Hkv, int Nq, int Nk, int d, float scale, int dtype,
+                              int num_splits, void* workspace, size_t ws_bytes, void* stream);
+
+/*
  * Bytes of device workspace fa_backward needs for these sizes: round_up(4 *
  * B*Hq*N, 256).  Returns 0 if the sizes are invalid.  Layout: D float32
  * [B, Hq, N] at offset 0, D_i = sum_c dO_ic * O_ic.
