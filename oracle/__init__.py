@@ -72,6 +72,10 @@ class Oracle:
         lib.oracle_backward.restype = i
         lib.oracle_forward_rect.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, i, i, ctypes.c_double]
         lib.oracle_forward_rect.restype = i
+        lib.oracle_forward_window.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, i, i, ctypes.c_double]
+        lib.oracle_forward_window.restype = i
+        lib.oracle_backward_window.argtypes = [dp] * 7 + [i] * 6 + [ctypes.c_double]
+        lib.oracle_backward_window.restype = i
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = i
         self.lib = lib
@@ -110,6 +114,33 @@ class Oracle:
         if rc != 0:
             raise ValueError(f"oracle_forward_rect failed with code {rc}")
         return o, lse
+
+    def forward_window(self, q, k, v, window: int, scale: float):
+        """Sliding-window causal forward: key k visible to query i iff i - window < k <= i."""
+        q, k, v = _as_f64(q), _as_f64(k), _as_f64(v)
+        B, Hq, N, d = q.shape
+        Hkv = k.shape[1]
+        assert k.shape == (B, Hkv, N, d) and v.shape == k.shape
+        o = np.empty_like(q)
+        lse = np.empty((B, Hq, N), dtype=np.float64)
+        rc = self.lib.oracle_forward_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                            B, Hq, Hkv, N, d, int(window), float(scale))
+        if rc != 0:
+            raise ValueError(f"oracle_forward_window failed with code {rc}")
+        return o, lse
+
+    def backward_window(self, q, k, v, dO, window: int, scale: float):
+        """Gradients of the sliding-window causal forward.  Returns (dq, dk, dv)."""
+        q, k, v, dO = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(dO)
+        B, Hq, N, d = q.shape
+        Hkv = k.shape[1]
+        dq, dk, dv = np.empty_like(q), np.empty_like(k), np.empty_like(v)
+        rc = self.lib.oracle_backward_window(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(dq),
+                                             _ptr(dk), _ptr(dv), B, Hq, Hkv, N, d, int(window),
+                                             float(scale))
+        if rc != 0:
+            raise ValueError(f"oracle_backward_window failed with code {rc}")
+        return dq, dk, dv
 
     def backward(self, q, k, v, dO, causal: bool, scale: float):
         """dQ, dK, dV (and D = rowsum(dO * O)) of the definition, fp64.
@@ -157,3 +188,13 @@ def backward(q, k, v, dO, causal: bool, scale: float):
 def forward_rect(q, k, v, scale: float):
     """See ``Oracle.forward_rect``."""
     return _default().forward_rect(q, k, v, scale)
+
+
+def forward_window(q, k, v, window: int, scale: float):
+    """See ``Oracle.forward_window``."""
+    return _default().forward_window(q, k, v, window, scale)
+
+
+def backward_window(q, k, v, dO, window: int, scale: float):
+    """See ``Oracle.backward_window``."""
+    return _default().backward_window(q, k, v, dO, window, scale)

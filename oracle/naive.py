@@ -25,13 +25,19 @@ def _expand_kv(x: np.ndarray, Hq: int) -> np.ndarray:
     return x[:, idx]
 
 
-def scores(q, k, scale, causal):
+def scores(q, k, scale, causal, window=None):
+    """Scores with future keys (causal) and, with a window W, keys more than
+    W - 1 positions in the past set to -inf."""
     q = np.asarray(q, dtype=np.float64)
     k = _expand_kv(np.asarray(k, dtype=np.float64), q.shape[1])
     s = scale * np.einsum("bhid,bhjd->bhij", q, k)
-    if causal:
+    if causal or window is not None:
         n = q.shape[2]
-        mask = np.triu(np.ones((n, n), dtype=bool), k=1)
+        i = np.arange(n)[:, None]
+        j = np.arange(n)[None, :]
+        mask = j > i
+        if window is not None:
+            mask |= j <= i - window
         s = np.where(mask, -np.inf, s)
     return s
 
@@ -42,8 +48,8 @@ def softmax(s):
     return e / e.sum(axis=-1, keepdims=True)
 
 
-def forward(q, k, v, causal, scale):
-    s = scores(q, k, scale, causal)
+def forward(q, k, v, causal, scale, window=None):
+    s = scores(q, k, scale, causal, window)
     p = softmax(s)
     vv = _expand_kv(np.asarray(v, dtype=np.float64), p.shape[1])
     o = np.einsum("bhij,bhjd->bhid", p, vv)
@@ -52,14 +58,14 @@ def forward(q, k, v, causal, scale):
     return o, lse, p
 
 
-def backward(q, k, v, dO, causal, scale):
+def backward(q, k, v, dO, causal, scale, window=None):
     q = np.asarray(q, dtype=np.float64)
     dO = np.asarray(dO, dtype=np.float64)
     B, Hq, N, d = q.shape
     Hkv = np.asarray(k).shape[1]
     kk = _expand_kv(np.asarray(k, dtype=np.float64), Hq)
     vv = _expand_kv(np.asarray(v, dtype=np.float64), Hq)
-    _, _, p = forward(q, k, v, causal, scale)
+    _, _, p = forward(q, k, v, causal, scale, window)
     dv_e = np.einsum("bhij,bhid->bhjd", p, dO)
     dp = np.einsum("bhid,bhjd->bhij", dO, vv)
     rs = (p * dp).sum(axis=-1, keepdims=True)

@@ -142,6 +142,119 @@ int oracle_forward(const double* q, const double* k, const double* v, double* o,
 }
 
 /*
+ * Sliding-window (local) causal attention: key k is visible to query i iff
+ * i - window < k <= i ("Flash Attention" (aiwiki.ai), section "Features":
+ * local sliding windows; block-sparse attention skips the blocks a mask
+ * leaves empty, section "Block-sparse FlashAttention").  window >= N is
+ * ordinary causal attention.  Layouts as for oracle_forward / oracle_backward.
+ */
+static double softmax_row_from(const double* qi, const double* kh, int k0, int k1, int d,
+                               double scale, double* p) {
+    /* p[0 .. k1-k0) over keys k0 .. k1-1 */
+    return softmax_row(qi, kh + (size_t)k0 * d, k1 - k0, d, scale, p);
+}
+
+int oracle_forward_window(const double* q, const double* k, const double* v, double* o,
+                          double* lse, int B, int Hq, int Hkv, int N, int d, int window,
+                          double scale) {
+    int rc = check_args(B, Hq, Hkv, N, d);
+    if (rc) return rc;
+    if (window < 1 || !q || !k || !v || !o || !lse) return ORACLE_EINVAL;
+    const int64_t rows = (int64_t)B * Hq * N;
+    int failed = 0;
+#pragma omp parallel
+    {
+        double* p = (double*)malloc(sizeof(double) * (size_t)N);
+        if (!p) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(dynamic, 16)
+        for (int64_t r = 0; r < rows; ++r) {
+            if (!p) continue;
+            const int i = (int)(r % N);
+            const int64_t bh = r / N;
+            const int h = (int)(bh % Hq);
+            const int b = (int)(bh / Hq);
+            const int g = (int)(((int64_t)h * Hkv) / Hq);
+            const double* kh = k + ((size_t)b * Hkv + g) * (size_t)N * d;
+            const double* vh = v + ((size_t)b * Hkv + g) * (size_t)N * d;
+            const int k0 = i - window + 1 > 0 ? i - window + 1 : 0;
+            lse[r] = softmax_row_from(q + (size_t)r * d, kh, k0, i + 1, d, scale, p);
+            double* oi = o + (size_t)r * d;
+            for (int c = 0; c < d; ++c) oi[c] = 0.0;
+            for (int kk = k0; kk <= i; ++kk)
+                for (int c = 0; c < d; ++c) oi[c] += p[kk - k0] * vh[(size_t)kk * d + c];
+        }
+        free(p);
+    }
+    return failed ? ORACLE_ENOMEM : ORACLE_OK;
+}
+
+int oracle_backward_window(const double* q, const double* k, const double* v, const double* dO,
+                           double* dq, double* dk, double* dv, int B, int Hq, int Hkv, int N,
+                           int d, int window, double scale) {
+    int rc = check_args(B, Hq, Hkv, N, d);
+    if (rc) return rc;
+    if (window < 1 || !q || !k || !v || !dO || !dq || !dk || !dv) return ORACLE_EINVAL;
+    const int group = Hq / Hkv;
+    const size_t nd = (size_t)N * d;
+    /* One KV head at a time, its group's rows in order (small sizes only). */
+    double* p = (double*)malloc(sizeof(double) * (size_t)N);
+    double* ds = (double*)malloc(sizeof(double) * (size_t)N);
+    double* oi = (double*)malloc(sizeof(double) * (size_t)d);
+    if (!p || !ds || !oi) {
+        free(p);
+        free(ds);
+        free(oi);
+        return ORACLE_ENOMEM;
+    }
+    for (int64_t bg = 0; bg < (int64_t)B * Hkv; ++bg) {
+        const int64_t b = bg / Hkv;
+        const int g = (int)(bg % Hkv);
+        const double* kh = k + (size_t)bg * nd;
+        const double* vh = v + (size_t)bg * nd;
+        double* dkh = dk + (size_t)bg * nd;
+        double* dvh = dv + (size_t)bg * nd;
+        memset(dkh, 0, sizeof(double) * nd);
+        memset(dvh, 0, sizeof(double) * nd);
+        for (int hh = 0; hh < group; ++hh) {
+            const int h = g * group + hh;
+            for (int i = 0; i < N; ++i) {
+                const size_t row = ((size_t)b * Hq + h) * (size_t)N + i;
+                const double* qi = q + row * d;
+                const double* doi = dO + row * d;
+                double* dqi = dq + row * d;
+                const int k0 = i - window + 1 > 0 ? i - window + 1 : 0;
+                const int nk = i + 1 - k0;
+                softmax_row_from(qi, kh, k0, i + 1, d, scale, p);
+                for (int c = 0; c < d; ++c) oi[c] = 0.0;
+                for (int t = 0; t < nk; ++t)
+                    for (int c = 0; c < d; ++c) oi[c] += p[t] * vh[(size_t)(k0 + t) * d + c];
+                const double Di = dot(doi, oi, d);
+                for (int t = 0; t < nk; ++t) ds[t] = p[t] * (dot(doi, vh + (size_t)(k0 + t) * d, d) - Di);
+                for (int c = 0; c < d; ++c) dqi[c] = 0.0;
+                for (int t = 0; t < nk; ++t)
+                    for (int c = 0; c < d; ++c) dqi[c] += ds[t] * kh[(size_t)(k0 + t) * d + c];
+                for (int c = 0; c < d; ++c) dqi[c] *= scale;
+                for (int t = 0; t < nk; ++t) {
+                    double* dkk = dkh + (size_t)(k0 + t) * d;
+                    double* dvk = dvh + (size_t)(k0 + t) * d;
+                    for (int c = 0; c < d; ++c) {
+                        dkk[c] += scale * ds[t] * qi[c];
+                        dvk[c] += p[t] * doi[c];
+                    }
+                }
+            }
+        }
+    }
+    free(p);
+    free(ds);
+    free(oi);
+    return ORACLE_OK;
+}
+
+/*
  * Forward with Nq query rows and Nk keys per head (non-causal): the same
  * definition with a rectangular score matrix, as used for decoding, where a
  * few new query rows attend to a long sequence of cached keys.

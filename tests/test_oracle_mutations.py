@@ -19,8 +19,10 @@ SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
 
 # (name, exact text in oracle.c, replacement)
 MUTATIONS = [
-    ("drop_D_term", "- Di);", ");"),
-    ("drop_dq_scale", "dqi[c] *= scale;", "dqi[c] *= 1.0;"),
+    ("drop_D_term", "(dot(doi, vh + (size_t)kk * d, d) - Di);", "(dot(doi, vh + (size_t)kk * d, d));"),
+    ("drop_dq_scale", "dqi[c] *= scale;\n                /* dK_k", "dqi[c] *= 1.0;\n                /* dK_k"),
+    ("window_backward_drops_D", "(dot(doi, vh + (size_t)(k0 + t) * d, d) - Di);",
+     "(dot(doi, vh + (size_t)(k0 + t) * d, d));"),
     ("dk_without_scale", "const double a = scale * ds[kk];", "const double a = ds[kk];"),
     ("dv_uses_q", "dvk[c] += w * doi[c];", "dvk[c] += w * qi[c];"),
     ("causal_off_by_one", "const int nk = causal ? i + 1 : N;\n            lse",
@@ -32,6 +34,9 @@ MUTATIONS = [
      "            const double* kh = k + ((size_t)b * Hkv + g) * (size_t)N * d;",
      "const int g = (int)(h % Hkv);\n            const double* qi = q + (size_t)r * d;\n"
      "            const double* kh = k + ((size_t)b * Hkv + g) * (size_t)N * d;"),
+    ("window_off_by_one",
+     "const int k0 = i - window + 1 > 0 ? i - window + 1 : 0;\n            lse[r]",
+     "const int k0 = i - window > 0 ? i - window : 0;\n            lse[r]"),
     ("rect_drops_last_key", "lse[r] = softmax_row(qi, kh, Nk, d, scale, p);",
      "lse[r] = softmax_row(qi, kh, Nk - 1, d, scale, p);"),
     ("unnormalised_p", "for (int k = 0; k < nk; ++k) p[k] /= l;", ""),
@@ -74,6 +79,19 @@ def _checks_fail(o: "oracle.Oracle") -> bool:
         for a, b in zip((dq, dk, dv), ref[:3]):
             if not np.allclose(a, b, atol=1e-9):
                 return True
+    # sliding window of 3 over 6 positions
+    qw, kw, vw = rng.standard_normal((B, Hq, 6, d)), rng.standard_normal((B, Hkv, 6, d)), \
+        rng.standard_normal((B, Hkv, 6, d))
+    o_w, l_w = o.forward_window(qw, kw, vw, 3, s)
+    o_n, l_n, _ = naive.forward(qw, kw, vw, True, s, window=3)
+    if not (np.allclose(o_w, o_n, atol=1e-9) and np.allclose(l_w, l_n, atol=1e-9)):
+        return True
+    dOw = rng.standard_normal((B, Hq, 6, d))
+    gw = o.backward_window(qw, kw, vw, dOw, 3, s)
+    gn = naive.backward(qw, kw, vw, dOw, True, s, window=3)
+    for a, b in zip(gw, gn[:3]):
+        if not np.allclose(a, b, atol=1e-9):
+            return True
     # rectangular (decoding) forward: 3 query rows against 9 keys
     qr, kr, vr = rng.standard_normal((B, Hq, 3, d)), rng.standard_normal((B, Hkv, 9, d)), \
         rng.standard_normal((B, Hkv, 9, d))

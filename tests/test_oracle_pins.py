@@ -258,3 +258,63 @@ def test_rect_forward_closed_forms_and_square_case():
     b, lb = oracle.forward(qs, ks, vs, False, 0.5)
     np.testing.assert_allclose(a, b, atol=1e-14)
     np.testing.assert_allclose(la, lb, atol=1e-14)
+
+
+# ---------------------------------------------------------------- sliding window
+@pytest.mark.parametrize("W", [1, 2, 5, 16])
+@pytest.mark.parametrize("B,Hq,Hkv,N,d", [(1, 1, 1, 9, 4), (2, 4, 2, 13, 8)])
+def test_window_bruteforce(W, B, Hq, Hkv, N, d):
+    q, k, v, dO = rand(B, Hq, N, d), rand(B, Hkv, N, d), rand(B, Hkv, N, d), rand(B, Hq, N, d)
+    o, lse = oracle.forward_window(q, k, v, W, 0.6)
+    o_n, lse_n, _ = naive.forward(q, k, v, True, 0.6, window=W)
+    np.testing.assert_allclose(o, o_n, atol=1e-12)
+    np.testing.assert_allclose(lse, lse_n, atol=1e-12)
+    g = oracle.backward_window(q, k, v, dO, W, 0.6)
+    r = naive.backward(q, k, v, dO, True, 0.6, window=W)
+    for a, b in zip(g, r[:3]):
+        np.testing.assert_allclose(a, b, atol=1e-12)
+
+
+def test_window_special_cases():
+    N, d, s = 10, 4, 0.7
+    q, k, v, dO = rand(1, 2, N, d), rand(1, 2, N, d), rand(1, 2, N, d), rand(1, 2, N, d)
+    # window >= N is causal attention
+    for W in (N, N + 7):
+        o, lse = oracle.forward_window(q, k, v, W, s)
+        oc, lc = oracle.forward(q, k, v, True, s)
+        np.testing.assert_allclose(o, oc, atol=1e-14)
+        np.testing.assert_allclose(lse, lc, atol=1e-14)
+        g = oracle.backward_window(q, k, v, dO, W, s)
+        gc = oracle.backward(q, k, v, dO, True, s)
+        for a, b in zip(g, gc[:3]):
+            np.testing.assert_allclose(a, b, atol=1e-12)
+    # window 1: every query sees only itself
+    o, lse = oracle.forward_window(q, k, v, 1, s)
+    np.testing.assert_array_equal(o, v)
+    np.testing.assert_allclose(lse, s * np.einsum("bhnd,bhnd->bhn", q, k), atol=1e-14)
+    dq, dk, dv = oracle.backward_window(q, k, v, dO, 1, s)
+    np.testing.assert_allclose(dq, 0.0, atol=1e-14)  # P = 1 exactly: no gradient through S
+    np.testing.assert_allclose(dv, dO, atol=1e-14)
+
+
+@pytest.mark.parametrize("W", [2, 3])
+def test_window_backward_finite_differences(W):
+    B, Hq, Hkv, N, d, s = 1, 2, 1, 6, 3, 0.9
+    q, k, v, dO = rand(B, Hq, N, d), rand(B, Hkv, N, d), rand(B, Hkv, N, d), rand(B, Hq, N, d)
+    dq, dk, dv = oracle.backward_window(q, k, v, dO, W, s)
+    h = 1e-6
+    for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        fd = np.zeros_like(x)
+        it = np.nditer(x, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            args = {"q": q, "k": k, "v": v}
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            args[name] = xp
+            lp = float((oracle.forward_window(args["q"], args["k"], args["v"], W, s)[0] * dO).sum())
+            args[name] = xm
+            lm = float((oracle.forward_window(args["q"], args["k"], args["v"], W, s)[0] * dO).sum())
+            fd[idx] = (lp - lm) / (2 * h)
+        np.testing.assert_allclose(g, fd, rtol=1e-6, atol=1e-7, err_msg=f"d{name}")
