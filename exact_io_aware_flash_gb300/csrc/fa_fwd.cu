@@ -97,7 +97,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, void* __restrict__ out,
                   float* __restrict__ lse_out, int heads, int head_group, int Hq, int Hkv, int N,
-                  int causal, int window, float scale_log2, int* err) {
+                  int causal, float scale_log2, int* err) {
   using L = FwdSmem<D>;
   constexpr int kAtoms = D / 64;
   extern __shared__ uint8_t smem_raw[];
@@ -120,19 +120,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kvh = b * Hkv + h / (Hq / Hkv);
   const int tA = 2 * pair, tB = 2 * pair + 1;
   const bool hasB = tB < T;
-  // Key tiles of query tile t: [key_lo(t), t] causal, [0, T) otherwise; with a
-  // sliding window the tiles wholly before the window of the tile's first row
-  // are skipped (block skipping generalised from the causal case).
-  auto key_lo = [&](int t) {
-    const int first = t * kBM - window + 1;
-    return (window > 0 && first > 0) ? first / kBN : 0;
-  };
-  const int loA = key_lo(tA);
-  const int loB = hasB ? key_lo(tB) : loA;
-  const int nA = (causal ? tA : T - 1) - loA + 1;
-  const int nB = hasB ? (causal ? tB : T - 1) - loB + 1 : 0;
-  const int offB = loB - loA;  // tile B's first key tile in the CTA's key stream
-  const int nKV = hasB ? offB + nB : nA;  // the CTA streams key tiles loA .. loA + nKV - 1
+  const int nA = causal ? tA + 1 : T;
+  const int nB = hasB ? (causal ? tB + 1 : T) : 0;
+  const int nKV = nA > nB ? nA : nB;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NBARS; ++i) {
@@ -178,13 +168,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_expect_tx(&bar[BKFULL + sk], L::kTile);
         for (int a = 0; a < kAtoms; ++a)
           tma_load_3d(smem + L::kK + sk * L::kTile + a * kAtomBytes, &tm_k, &bar[BKFULL + sk],
-                      a * 64, (loA + j) * kBN, kvh, pol_kv);
+                      a * 64, j * kBN, kvh, pol_kv);
         kissued = j + 1;
         if (!mbar_wait(&bar[BVEMPTY + sv], pv ^ 1, abort_flag, err)) break;
         mbar_expect_tx(&bar[BVFULL + sv], L::kTile);
         for (int a = 0; a < kAtoms; ++a)
           tma_load_3d(smem + L::kV + sv * L::kTile + a * kAtomBytes, &tm_v, &bar[BVFULL + sv],
-                      a * 64, (loA + j) * kBN, kvh, pol_kv);
+                      a * 64, j * kBN, kvh, pol_kv);
         vissued = j + 1;
       }
       if (*abort_flag) {
@@ -208,7 +198,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const int X = warp - 9;
       const int nX = X ? nB : nA;
-      const int off = X ? offB : 0;  // this tile's first position in the key stream
       constexpr uint32_t kIdS = idesc_f16(kBM, kBN, BF16, false, false);
       constexpr uint32_t kIdO = idesc_f16(kBM, D, BF16, false, true);
       const uint32_t qa = smem_u32(smem + L::kQ) + X * L::kTile;
@@ -228,61 +217,53 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(&bar[BSFULL + X]);
         mma_commit(&bar[BKEMPTY + stk]);
       };
-      auto issue_pv = [&](int stv, int jl) {
+      auto issue_pv = [&](int stv, int j) {
         const uint32_t va = sv + stv * L::kTile;
 #pragma unroll
         for (int ks = 0; ks < kBN / 16; ++ks)
           mma_ts(tO, tS + ks * 8, sdesc_sw128(va + ks * 2048, kAtomBytes, 1024), kIdO,
-                 (jl > 0 || ks > 0) ? 1u : 0u);
+                 (j > 0 || ks > 0) ? 1u : 0u);
         mma_commit(&bar[BODONE + X]);
         mma_commit(&bar[BVEMPTY + stv]);
       };
 
-      // Key tiles of the stream this query tile does not visit (before its
-      // window starts, or after its diagonal) still need this issuer's release.
-      // Its arrival for a use of a stage may only come after that stage's
-      // previous use has been released by both issuers.
-      auto release = [&](int g) {
-        const int stk = g % kKStages;
-        const int stv = g % kVStages;
-        if (g >= kKStages &&
-            !mbar_wait(&bar[BKEMPTY + stk], ((g / kKStages) - 1) & 1, abort_flag, err))
-          return false;
-        if (g >= kVStages &&
-            !mbar_wait(&bar[BVEMPTY + stv], ((g / kVStages) - 1) & 1, abort_flag, err))
-          return false;
-        mbar_arrive(&bar[BKEMPTY + stk]);
-        mbar_arrive(&bar[BVEMPTY + stv]);
-        return true;
-      };
       bool ok = true;
-      for (int g = 0; ok && g < off; ++g) ok = release(g);
-      if (ok && nX > 0) {
-        ok = mbar_wait(&bar[BQ], 0, abort_flag, err) &&
-             mbar_wait(&bar[BKFULL + off % kKStages], (off / kKStages) & 1, abort_flag, err);
+      if (nX > 0) {
+        ok = mbar_wait(&bar[BQ], 0, abort_flag, err) && mbar_wait(&bar[BKFULL], 0, abort_flag, err);
         if (ok) {
           tc_fence_after();
-          issue_s(off % kKStages);
+          issue_s(0);
         }
       }
-      // jl: this tile's own count (phases of its S, P, O barriers); g = off + jl:
-      // position in the key stream (stages and phases of the K/V rings).
-      for (int jl = 0; ok && jl < nX; ++jl) {
-        const int g = off + jl;
-        const int stv = g % kVStages;
-        if (!(ok = mbar_wait(&bar[BVFULL + stv], (g / kVStages) & 1, abort_flag, err))) break;
-        if (!(ok = mbar_wait(&bar[BPFULL + X], jl & 1, abort_flag, err))) break;
+      for (int j = 0; ok && j < nX; ++j) {
+        const int stv = j % kVStages;
+        if (!(ok = mbar_wait(&bar[BVFULL + stv], (j / kVStages) & 1, abort_flag, err))) break;
+        if (!(ok = mbar_wait(&bar[BPFULL + X], j & 1, abort_flag, err))) break;
         tc_fence_after();
-        issue_pv(stv, jl);
-        if (jl + 1 < nX) {
-          const int stk1 = (g + 1) % kKStages;
-          if (!(ok = mbar_wait(&bar[BKFULL + stk1], ((g + 1) / kKStages) & 1, abort_flag, err))) break;
-          if (!(ok = mbar_wait(&bar[BODONE + X], jl & 1, abort_flag, err))) break;
+        issue_pv(stv, j);
+        if (j + 1 < nX) {
+          const int stk1 = (j + 1) % kKStages;
+          if (!(ok = mbar_wait(&bar[BKFULL + stk1], ((j + 1) / kKStages) & 1, abort_flag, err))) break;
+          if (!(ok = mbar_wait(&bar[BODONE + X], j & 1, abort_flag, err))) break;
           tc_fence_after();
           issue_s(stk1);
         }
       }
-      for (int g = off + nX; ok && g < nKV; ++g) ok = release(g);
+      // Key tiles this query tile does not visit still need this issuer's
+      // release.  Its arrival for a use of a stage may only come after that
+      // stage's previous use has been released by both issuers.
+      for (int j = nX; ok && j < nKV; ++j) {
+        const int stk = j % kKStages;
+        const int stv = j % kVStages;
+        if (j >= kKStages && !(ok = mbar_wait(&bar[BKEMPTY + stk], ((j / kKStages) - 1) & 1,
+                                              abort_flag, err)))
+          break;
+        if (j >= kVStages && !(ok = mbar_wait(&bar[BVEMPTY + stv], ((j / kVStages) - 1) & 1,
+                                              abort_flag, err)))
+          break;
+        mbar_arrive(&bar[BKEMPTY + stk]);
+        mbar_arrive(&bar[BVEMPTY + stv]);
+      }
       // Every MMA this thread issued has completed before TMEM is released.
       mma_commit(&bar[BFINAL + X]);
       drain_wait(&bar[BFINAL + X], 0);
@@ -292,7 +273,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int X = warp >> 2;
     const int t = X ? tB : tA;
     const int nX = X ? nB : nA;
-    const int lo = X ? loB : loA;  // this tile's first key tile
     const int r = threadIdx.x & 127;
     const int q = t * kBM + r;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -303,17 +283,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool pos_scale = scale_log2 > 0.f;
     const float sfac = pos_scale ? scale_log2 : 1.0f;
     bool ok = true;
-    for (int jl = 0; jl < nX; ++jl) {
-      // The two tiles' softmaxes take turns over the key stream -- A(0), B(0),
-      // A(1), B(1), ... -- so each runs alone on the SM's ALUs while the tensor
-      // core works on the other tile.  A at stream position g follows B at
-      // g - 1, and B at g follows A at g, where the other tile visits them.
-      const int g = (X ? offB : 0) + jl;
+    for (int j = 0; j < nX; ++j) {
+      // The two tiles' softmaxes take turns -- A(0), B(0), A(1), B(1), ... -- so
+      // each runs alone on the SM's ALUs while the tensor core works on the
+      // other tile.  A(j) follows B(j-1); B(j) follows A(j) where tile A has one.
       bool turn = true;
-      if (X == 0 && g - 1 >= offB && g - 1 < offB + nB)
-        turn = mbar_wait(&bar[BPFULL + 1], (g - 1 - offB) & 1, abort_flag, err);
-      if (X == 1 && g < nA) turn = mbar_wait(&bar[BPFULL], g & 1, abort_flag, err);
-      ok = __all_sync(0xffffffffu, turn && mbar_wait(&bar[BSFULL + X], jl & 1, abort_flag, err));
+      if (X == 0 && j > 0 && nB > 0) turn = mbar_wait(&bar[BPFULL + 1], (j - 1) & 1, abort_flag, err);
+      if (X == 1 && j < nA) turn = mbar_wait(&bar[BPFULL], j & 1, abort_flag, err);
+      ok = __all_sync(0xffffffffu, turn && mbar_wait(&bar[BSFULL + X], j & 1, abort_flag, err));
       if (!ok) break;
       tc_fence_after();
       // x holds the scores as raw bits: s * scale * log2(e) after the first pass.
@@ -322,11 +299,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < kBN; c += 32) tmem_ld32(tS + c, x + c);
       tmem_ld_wait();
       reg_fence<kBN>(x);
-      const int jkey = lo + jl;  // key tile
-      const int kbase = jkey * kBN;
-      const bool diag = causal && (jkey == t);
-      // first key this row may see under the sliding window, relative to the tile
-      const int c_lo = window > 0 ? q - window + 1 - kbase : -1;
+      const int kbase = j * kBN;
+      const bool diag = causal && (j == t);
       // Scores stay raw when scale > 0 (the exponent is then one FFMA,
       // s * scale*log2(e) - m, and the row maximum of raw scores times the
       // positive factor is the maximum of the scaled scores); for scale <= 0
@@ -341,11 +315,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < kBN; ++c)
           if (c >= lim) x[c] = __float_as_uint(-INFINITY);
-      }
-      if (__any_sync(0xffffffffu, c_lo > 0)) {  // keys before the window start
-#pragma unroll
-        for (int c = 0; c < kBN; ++c)
-          if (c < c_lo) x[c] = __float_as_uint(-INFINITY);
       }
       // row maximum as eight independent chains, then a tree
       // eight chains (chain u: scores u, u+8, ..., u+120) of three-input maxima
@@ -364,8 +333,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // (p <= 2^8 then); the decision is warp-uniform because TMEM access is.
       float alpha = 1.0f;
       bool rescale = false;
-      if (jl == 0) {
-        m_run = mx;  // -inf for a row whose window starts in a later tile
+      if (j == 0) {
+        m_run = mx;
       } else {
         const bool need = mx > m_run + 8.0f;
         rescale = __any_sync(0xffffffffu, need);
@@ -376,9 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // exponent arguments and row sums two at a time (packed fp32)
       const uint64_t sfac2 = f2_pack(sfac, sfac);
-      // A row that has seen no key yet has m_run = -inf; its P is 0 either way.
-      const float m_use = m_run == -INFINITY ? 0.f : m_run;
-      const uint64_t negm2 = f2_pack(-m_use, -m_use);
+      const uint64_t negm2 = f2_pack(-m_run, -m_run);
       uint64_t rs2[2] = {0ull, 0ull};
 #pragma unroll
       for (int c = 0; c < kBN; c += 32) {
@@ -474,7 +441,7 @@ cudaError_t launch_fwd_t(const AttnShape& s, const FwdArgs& a, cudaStream_t stre
   hg = hg < 1 ? 1 : (hg > 64 ? 64 : hg);
   kern<<<grid, kThreads, smem, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.o, a.lse, s.B * s.Hq,
                                          static_cast<int>(hg), s.Hq, s.Hkv, s.N, s.causal,
-                                         s.window, scale_log2, a.err);
+                                         scale_log2, a.err);
   return cudaGetLastError();
 }
 
