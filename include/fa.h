@@ -148,8 +148,10 @@ FA_API int fa_backward(const void* q, const void* k, const void* v, const void* 
  * Same arguments, outputs, errors and asynchrony as fa_backward, minus the
  * workspace: the scratch fa_backward needs (the D vector,
  * fa_backward_workspace_size() bytes) is taken from one
- * FA_NOALLOC_SCRATCH_BYTES-byte array compiled into the library's device code,
- * which every GPU that loads the library holds until the process exits.  It is
+ * FA_NOALLOC_SCRATCH_BYTES-byte array compiled into the library's device code.
+ * The array is placed in device memory on the first call on each device (the
+ * runtime loads the library's device code lazily) and stays there until the
+ * process exits.  It is
  * for callers that may not call cudaMalloc or any other allocator: a host
  * program that reserves all device memory up front and forbids allocation
  * afterwards, a plugin running inside a framework that gives it no allocator,
@@ -159,8 +161,11 @@ FA_API int fa_backward(const void* q, const void* k, const void* v, const void* 
  * - Sizes whose fa_backward_workspace_size() exceeds FA_NOALLOC_SCRATCH_BYTES
  *   are rejected with FA_ERR_UNSUPPORTED (nothing is enqueued); use
  *   fa_backward with a workspace for those.
- * - The first call on each device looks up the array's device address with
- *   that device current; make that first call before any stream capture.
+ * - The first call on each device places the array and looks up its device
+ *   address, with that device current.  Make that first call before the
+ *   caller reserves the rest of the device's memory and before any stream
+ *   capture.  If it fails (FA_ERR_CUDA, e.g. no memory left to place the
+ *   array) nothing is enqueued and a later call tries again.
  * - Every call on a device shares the one array and leaves its contents
  *   behind; each call overwrites every element it later reads, so nothing
  *   has to start at zero.  Calls whose GPU work overlaps (different streams, or
