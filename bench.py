@@ -10,7 +10,13 @@ run forward then backward as in a training step.  Each of Q, K, V, O, dO is
 Metric: attention fwd+bwd TFLOPS, algorithmic FLOPs (forward 4*B*H*N^2*d halved
 for causal, backward 2.5x that) divided by device time.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--sweep]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--skip-workloads] [--no-cpu-baseline]
+
+Besides the step's own numbers, the line carries `workloads`: the device time
+and throughput of every evaluation workload (the four forward workloads, with
+% of HBM for the two short-N ones, and every point of the backward sweep),
+and `roofline` for the backward's two main kernels on the method's 5 products.
 
 With torchrun (N>1) every rank runs its own replica of the workload (the op has
 no cross-GPU exchange) and rank 0 prints the whole-job throughput.
@@ -25,8 +31,10 @@ import json
 import math
 import os
 import statistics
+import shutil
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -94,10 +102,10 @@ class ClockSampler:
     def __init__(self, gpu_id: str):
         self.gpu_id = gpu_id
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        self.dir = tempfile.mkdtemp(prefix="fa_bench_clocks_")
+        self.path = os.path.join(self.dir, "clocks.csv")
 
     def start(self):
-        os.makedirs(os.path.dirname(self.path), exist_ok=True)
         try:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
@@ -131,6 +139,7 @@ class ClockSampler:
                 for n, v in zip(names, parts[5:9]):
                     if v.lower().startswith("active"):
                         reasons.add(n)
+        shutil.rmtree(self.dir, ignore_errors=True)
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
                 "samples": len(sm), "reasons": sorted(reasons)}
@@ -162,6 +171,12 @@ def recorded_traffic(kernel: str):
     if d.get("sources_digest") != kernel_sources_digest(kernel):
         return None
     return d.get("dram_bytes_per_launch_full_workload")
+
+
+def recorded_traffic_sum(kernels):
+    """Summed DRAM bytes of one launch of each kernel, or None if any record is stale."""
+    parts = [recorded_traffic(k) for k in kernels]
+    return None if any(p is None for p in parts) else float(sum(parts))
 
 
 # ------------------------------------------------------------------ CPU oracle
@@ -372,19 +387,18 @@ def run_ours(args):
     if rank == 0:
         peaks, peak_kind = load_peaks()
         peak = peaks["bf16_tflops_sustained"]
-        # Algorithmic FLOPs of each kernel: the N x N x d products it performs
-        # (forward 2: S, PV; dK/dV 4: S^T, dP^T, dV, dK; dQ 3: S, dP, dQ), each
-        # 2*B*H*N^2*d halved for causal.
+        # Algorithmic FLOPs: the method's own products, each 2*B*H*N^2*d halved
+        # for causal -- forward 2 (S = Q K^T, O += P V), backward 5 (S, dP, dV,
+        # dK, dQ).  The backward's two kernels recompute S and dP in both passes
+        # (7 products performed); that recompute is not counted as work.
         per_product = f_fwd / 2.0
-        kernels = {
-            "fa_fwd_kernel": (fwd_ms, 2 * per_product, "2 products: S = Q K^T, O += P V"),
-            "fa_bwd_dkdv_kernel": (dkdv_ms, 4 * per_product,
-                                   "4 products: S^T, dP^T, dV += P^T dO, dK += dS^T Q"),
-            "fa_bwd_dq_kernel": (dq_ms, 3 * per_product, "3 products: S, dP, dQ += dS K"),
+        bwd_main_ms = dkdv_ms + dq_ms
+        achieved = f_bwd / (bwd_main_ms * 1e-3) / 1e12
+        own = {  # products each kernel performs, for context
+            "fa_fwd_kernel": (fwd_ms, 2, "S = Q K^T, O += P V"),
+            "fa_bwd_dkdv_kernel": (dkdv_ms, 4, "S^T, dP^T, dV += P^T dO, dK += dS^T Q"),
+            "fa_bwd_dq_kernel": (dq_ms, 3, "S, dP, dQ += dS K"),
         }
-        dom = max(kernels, key=lambda k: kernels[k][0])
-        dom_ms, dom_flops, dom_what = kernels[dom]
-        achieved = dom_flops / (dom_ms * 1e-3) / 1e12
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": elapsed_ms / K, "higher_is_better": True,
@@ -396,28 +410,40 @@ def run_ours(args):
                                  "peaks": peak_kind},
             "components": {
                 "forward": {"ms": fwd_ms, "tflops": f_fwd / (fwd_ms * 1e-3) / 1e12,
+                            "pct_of_bf16_burst": f_fwd / (fwd_ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
                             "kernel": "fa_fwd_kernel"},
                 "backward": {"ms": bwd_ms, "tflops": f_bwd / (bwd_ms * 1e-3) / 1e12,
+                             "pct_of_bf16_burst": f_bwd / (bwd_ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
                              "dkdv_kernel_ms": dkdv_ms, "dq_kernel_ms": dq_ms,
                              "kernels": ["fa_bwd_pre_kernel", "fa_bwd_dkdv_kernel", "fa_bwd_dq_kernel"],
                              "note": "TFLOPS counts the 5 products of the gradient; the kernels "
                                      "recompute S and dP in both passes (7 products)"},
             },
             "roofline": {
-                "kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak,
-                "unit": "TFLOP/s", "frac": achieved / peak,
-                "peak_kind": f"{peak_kind} bf16 sustained (kernel timed inside a long step)",
+                "kernel": "fa_bwd_dkdv_kernel + fa_bwd_dq_kernel (the backward's two main "
+                          "kernels, together the largest share of device time)",
+                "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak,
+                "peak_kind": f"{peak_kind} bf16 sustained (kernels timed inside a long step)",
                 "frac_of_burst": achieved / peaks["bf16_tflops"],
-                "traffic": recorded_traffic(dom),
-                "algorithmic": f"{dom_what}; each 2*B*H*N^2*d/2 FLOPs (causal); "
-                               f"{dom_flops / 1e9:.1f} GFLOP per launch",
-                "per_kernel_tflops": {k: v[1] / (v[0] * 1e-3) / 1e12 for k, v in kernels.items()},
+                "traffic": recorded_traffic_sum(("fa_bwd_dkdv_kernel", "fa_bwd_dq_kernel")),
+                "algorithmic": f"the method's 5 backward products (S, dP, dV, dK, dQ), each "
+                               f"2*B*H*N^2*d/2 FLOPs (causal): {f_bwd / 1e9:.1f} GFLOP per "
+                               f"backward, over the two kernels' summed mean launch time "
+                               f"{bwd_main_ms:.4f} ms (CUDA events on the launching stream)",
+                "per_kernel": {k: {"ms": v[0], "products_performed": v[1], "what": v[2],
+                                   "tflops_on_products_performed":
+                                       v[1] * per_product / (v[0] * 1e-3) / 1e12,
+                                   "traffic": recorded_traffic(k)}
+                               for k, v in own.items()},
             },
             "clocks": clocks,
             "e2e": {"value": e2e_value, "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": E},
             "gpu_launches": 4 * K,
         }
+        if not args.skip_workloads:
+            line["workloads"] = workload_table(dev, peaks)
         if world == 1 and not args.no_cpu_baseline:
             fl, secs, heads, threads = cpu_oracle_sample(budget_s=12.0, max_heads=64)
             line["cpu_baseline"] = {
@@ -425,69 +451,117 @@ def run_ours(args):
                 "sample": f"{heads} full head(s) (b=0, h=0 inputs) of the workload, N={WORKLOAD['N']}, "
                           f"fp64 forward + backward, {secs:.1f} s"}
         print(json.dumps(line), flush=True)
-        if args.sweep:
-            sweep(dev)
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
     return 0
 
 
-def sweep(dev):
-    """Extra lines (not the bench line): forward workloads and the backward sweep."""
+def _graph_time(fn, iters=20):
+    """Device time per call: `iters` back-to-back calls captured in a CUDA graph
+    and replayed, so host-side launch cost does not enter small cases."""
     import torch
 
-    from exact_io_aware_flash_gb300 import (backward, check_errors, forward, forward_splitkv,
-                                            workspace_size)
-    from exact_io_aware_flash_gb300.flops import backward_flops, forward_flops
+    from exact_io_aware_flash_gb300 import check_errors
+
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    check_errors()
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            for _ in range(iters):
+                fn()
+    torch.cuda.current_stream().wait_stream(side)
+    graph.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    graph.replay()
+    b.record()
+    torch.cuda.synchronize()
+    check_errors()
+    return a.elapsed_time(b) / iters
+
+
+def _cold_l2_time(fn, flush, iters=20):
+    """Median device time of one call that follows an L2 flush (a write larger
+    than the L2), each call bracketed by its own CUDA events."""
+    import torch
+
+    from exact_io_aware_flash_gb300 import check_errors
+
+    fn()
+    times = []
+    for _ in range(iters):
+        flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    check_errors()
+    return statistics.median(times)
+
+
+# targets of the evaluation: forward >= 60% of the bf16 peak on the two large
+# forward workloads, backward >= 45% at N >= 4096
+FWD_TARGET, BWD_TARGET = 0.60, 0.45
+
+
+def workload_table(dev, peaks):
+    """Device time and throughput of every evaluation workload: the four forward
+    workloads (with % of HBM for the two short-N ones) and the backward sweep."""
+    import torch
+
+    from exact_io_aware_flash_gb300 import backward, forward, forward_splitkv, workspace_size
+    from exact_io_aware_flash_gb300.flops import backward_flops, forward_bytes, forward_flops
     from exact_io_aware_flash_gb300.synth import (BACKWARD_SWEEP_N, WORKLOADS, backward_sweep_shape,
                                                   make_inputs)
 
-    def timed(fn, iters=20):
-        """Device time per call: `iters` calls captured in a CUDA graph and replayed,
-        so host-side launch cost does not enter small cases."""
-        for _ in range(3):
-            fn()
-        torch.cuda.synchronize()
-        check_errors()
-        graph = torch.cuda.CUDAGraph()
-        side = torch.cuda.Stream()
-        side.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(side):
-            with torch.cuda.graph(graph, stream=side):
-                for _ in range(iters):
-                    fn()
-        torch.cuda.current_stream().wait_stream(side)
-        graph.replay()
-        torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        graph.replay()
-        b.record()
-        torch.cuda.synchronize()
-        check_errors()
-        return a.elapsed_time(b) / iters
-
+    burst = peaks["bf16_tflops"]
+    hbm = peaks["hbm_gbs"]
+    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = lambda: flush_buf.fill_(1)
+    out = {"timing": "forward and backward: back-to-back launches replayed from a CUDA graph "
+                     "(device time per call); short-N forward also with a 256 MB L2 flush "
+                     "before each call (median of per-call CUDA events)",
+           "peaks": {"bf16_tflops_burst": burst, "hbm_gbs": hbm}}
+    fwd = {}
     for name, wl in WORKLOADS.items():
         s = wl["shape"]
         inp = make_inputs(s, wl["dtype"], seed=wl["seed"], with_dO=False)
         q, k, v = (inp[n].to(dev) for n in ("q", "k", "v"))
+        o = torch.empty_like(q)
+        lse = torch.empty(s.B, s.Hq, s.N, dtype=torch.float32, device=dev)
+        short = s.N <= 1024
         for causal in wl["causal"]:
-            ms = timed(lambda: forward(q, k, v, causal=causal))
+            call = lambda: forward(q, k, v, causal=causal, out=o, lse=lse)
+            ms = _graph_time(call)
             fl = forward_flops(s.B, s.Hq, s.N, s.d, causal)
-            print(json.dumps({"sweep": "forward", "workload": name, "causal": causal, "ms": ms,
-                              "tflops": fl / ms / 1e9}), flush=True)
-    # decoding: one new query row per head against a 32k-token cache (GQA 32/8)
-    B, Hq, Hkv, Nk, d = 8, 32, 8, 32768, 128
-    qd = torch.randn(B, Hq, 1, d, device=dev, dtype=torch.bfloat16)
-    kd = torch.randn(B, Hkv, Nk, d, device=dev, dtype=torch.bfloat16)
-    vd = torch.randn_like(kd)
-    ms = timed(lambda: forward_splitkv(qd, kd, vd))
-    kv_bytes = 2 * kd.numel() * kd.element_size()
-    peaks, _ = load_peaks()
-    print(json.dumps({"sweep": "decode", "B": B, "Hq": Hq, "Hkv": Hkv, "Nq": 1, "Nk": Nk, "d": d,
-                      "ms": ms, "kv_gbs": kv_bytes / ms / 1e6,
-                      "frac_of_hbm": kv_bytes / ms / 1e6 / peaks["hbm_gbs"]}), flush=True)
+            e = {"shape": f"B{s.B} Hq{s.Hq} Hkv{s.Hkv} N{s.N} d{s.d} {wl['dtype']}",
+                 "causal": causal, "ms": ms, "tflops": fl / ms / 1e9,
+                 "pct_of_bf16_burst": fl / ms / 1e9 / burst}
+            if short:
+                nbytes = forward_bytes(s.B, s.Hq, s.Hkv, s.N, s.d)
+                ms_cold = _cold_l2_time(call, flush)
+                e.update({"algorithmic_bytes": nbytes,
+                          "hbm_gbs_warm_l2": nbytes / ms / 1e6,
+                          "frac_of_hbm_warm_l2": nbytes / ms / 1e6 / hbm,
+                          "ms_cold_l2": ms_cold,
+                          "hbm_gbs_cold_l2": nbytes / ms_cold / 1e6,
+                          "frac_of_hbm_cold_l2": nbytes / ms_cold / 1e6 / hbm})
+            else:
+                e.update({"target_pct": FWD_TARGET,
+                          "target_met": fl / ms / 1e9 / burst >= FWD_TARGET})
+            fwd[f"{name}{'_causal' if causal and 'causal' not in name else ''}"] = e
+        del q, k, v, o, lse
+    out["forward"] = fwd
+    bwd = {}
     for N in BACKWARD_SWEEP_N:
         s = backward_sweep_shape(N)
         inp = make_inputs(s, "bf16", seed=1005 + N)
@@ -495,11 +569,28 @@ def sweep(dev):
         o, lse = forward(q, k, v, causal=True)
         ws = torch.empty(workspace_size(s.B, s.Hq, s.N, s.d), dtype=torch.uint8, device=dev)
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-        ms = timed(lambda: backward(q, k, v, o, lse, dO, causal=True, dq=dq, dk=dk, dv=dv,
-                                    workspace=ws), iters=10)
+        ms = _graph_time(lambda: backward(q, k, v, o, lse, dO, causal=True, dq=dq, dk=dk, dv=dv,
+                                          workspace=ws), iters=10)
         fl = backward_flops(s.B, s.Hq, s.N, s.d, True)
-        print(json.dumps({"sweep": "backward", "B": s.B, "H": s.Hq, "N": N, "d": 128,
-                          "ms": ms, "tflops": fl / ms / 1e9}), flush=True)
+        e = {"shape": f"B{s.B} H{s.Hq} N{N} d{s.d} bf16 causal", "ms": ms,
+             "tflops": fl / ms / 1e9, "pct_of_bf16_burst": fl / ms / 1e9 / burst}
+        if N >= 4096:
+            e.update({"target_pct": BWD_TARGET, "target_met": fl / ms / 1e9 / burst >= BWD_TARGET})
+        bwd[f"N{N}"] = e
+        del q, k, v, dO, o, lse, ws, dq, dk, dv
+    out["backward_sweep"] = bwd
+    # decoding (split-KV): one new query row per head against a 32k-token cache, GQA 32/8
+    B, Hq, Hkv, Nk, d = 8, 32, 8, 32768, 128
+    g = torch.Generator(device="cpu").manual_seed(4096)
+    qd = torch.randn(B, Hq, 1, d, generator=g).to(torch.bfloat16).to(dev)
+    kd = torch.randn(B, Hkv, Nk, d, generator=g).to(torch.bfloat16).to(dev)
+    vd = torch.randn(B, Hkv, Nk, d, generator=g).to(torch.bfloat16).to(dev)
+    ms = _graph_time(lambda: forward_splitkv(qd, kd, vd))
+    kv_bytes = 2 * kd.numel() * kd.element_size()
+    out["decode_splitkv"] = {"shape": f"B{B} Hq{Hq} Hkv{Hkv} Nq1 Nk{Nk} d{d} bf16", "ms": ms,
+                             "kv_gbs": kv_bytes / ms / 1e6,
+                             "frac_of_hbm": kv_bytes / ms / 1e6 / hbm}
+    return out
 
 
 def main():
@@ -508,7 +599,8 @@ def main():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--sweep", action="store_true", help="also print per-workload lines")
+    ap.add_argument("--skip-workloads", action="store_true",
+                    help="leave the per-workload table out of the line (for profiler runs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -777,7 +777,7 @@ int l2_head_group(long per_head_bytes) {
 
 int grid_for(long work_items, int per_block) {
   long blocks = (work_items + per_block - 1) / per_block;
-  const long cap = 152L * 16;  // 16 resident 256-thread blocks per SM
+  const long cap = static_cast<long>(sm_count()) * 16;  // 16 resident 256-thread blocks per SM
   if (blocks > cap) blocks = cap;
   return static_cast<int>(blocks < 1 ? 1 : blocks);
 }

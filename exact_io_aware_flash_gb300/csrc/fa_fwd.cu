@@ -10,9 +10,10 @@
 // end, "Flash Attention", section "Online softmax").
 //
 // GB300 design (one CTA per pair of 128-row query tiles of one head):
-//   warp 8      TMA producer: Q tiles once, then K_j and V_j through two
-//               2-stage shared-memory rings (128-byte swizzle, 3-D tensor maps
-//               over [B*H, N, d] so ragged tails are zero-filled).
+//   warp 8      TMA producer: Q tiles once, then K_j through a 3-stage and
+//               V_j through a 2-stage shared-memory ring (128-byte swizzle,
+//               3-D tensor maps over [B*H, N, d] so ragged tails are
+//               zero-filled).
 //   warps 9-10  MMA issuers, one thread per query tile X: S_X = Q_X K_j^T into
 //               Tensor Memory, O_X += P_X V_j with P_X read from Tensor Memory
 //               (A operand) and V_j from shared memory as an MN-major B operand.

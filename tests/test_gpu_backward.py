@@ -103,17 +103,49 @@ def test_backward_is_deterministic():
     assert torch.equal(dq1, dq2) and torch.equal(dk1, dk2) and torch.equal(dv1, dv2)
 
 
+def spread_heads(B, H, count=8):
+    """`count` (b, h) pairs evenly spaced over the linear head index b*H + h,
+    first and last included.  The kernels take heads in groups of consecutive
+    linear indices (sized to the L2), so this touches every part of the launch
+    order, the last (possibly partial) group included."""
+    n = B * H
+    idx = sorted({round(i * (n - 1) / (count - 1)) for i in range(count)}) if n > 1 else [0]
+    return [(x // H, x % H) for x in idx]
+
+
 @pytest.mark.parametrize("N", BACKWARD_SWEEP_N)
 def test_backward_sweep_workload(N):
-    """H=16, d=128, bf16, causal, B*N = 32768: full-size GPU run, oracle on sampled heads."""
+    """H=16, d=128, bf16, causal, B*N = 32768: full-size GPU run, oracle on 8 heads
+    spread over the launch order."""
     shape = backward_sweep_shape(N)
     inp = make_inputs(shape, "bf16", seed=1005 + N)
     scale = 1.0 / math.sqrt(128)
     _, _, dq, dk, dv = gpu_fwd_bwd(inp, True, scale)
-    for b, h in ((0, 0), (shape.B - 1, 15)):
+    for b, h in spread_heads(shape.B, shape.Hq):
         sl = lambda t: t[b:b + 1, h:h + 1]
         dq_r, dk_r, dv_r, _ = oracle.backward(sl(inp["q"]), sl(inp["k"]), sl(inp["v"]),
                                               sl(inp["dO"]), True, scale)
         for name, g, r in (("dq", sl(dq), dq_r), ("dk", sl(dk), dk_r), ("dv", sl(dv), dv_r)):
             e = rel_fro(g, r)
             assert e <= TOL_REL, f"N={N} head ({b},{h}) {name}: {e:.3g}"
+
+
+@pytest.mark.parametrize("kv_heads", [(0, 0), (0, 7)])
+def test_backward_gqa_at_size(kv_heads):
+    """GQA backward on a shape with several head groups and many tiles per head:
+    B=1, Hq=32, Hkv=8 (groups of 4), N=4096, d=128, bf16, causal.  For each
+    checked KV head the oracle takes its whole query group, so dK and dV are the
+    sums over the group's 4 query heads, and dQ is checked for those 4 heads."""
+    shape = Shape(1, 32, 8, 4096, 128)
+    inp = make_inputs(shape, "bf16", seed=2718)
+    scale = 1.0 / math.sqrt(128)
+    _, _, dq, dk, dv = gpu_fwd_bwd(inp, True, scale)
+    g = shape.group
+    for b, hk in (kv_heads,):
+        qs = lambda t: t[b:b + 1, hk * g:(hk + 1) * g]
+        ks = lambda t: t[b:b + 1, hk:hk + 1]
+        dq_r, dk_r, dv_r, _ = oracle.backward(qs(inp["q"]), ks(inp["k"]), ks(inp["v"]),
+                                              qs(inp["dO"]), True, scale)
+        for name, gg, r in (("dq", qs(dq), dq_r), ("dk", ks(dk), dk_r), ("dv", ks(dv), dv_r)):
+            e = rel_fro(gg, r)
+            assert e <= TOL_REL, f"GQA KV head ({b},{hk}) {name}: {e:.3g}"
