@@ -43,11 +43,19 @@ namespace {
 constexpr int kBM = 128;           // query rows per tile
 constexpr int kBN = 128;           // keys per tile
 constexpr int kAtomBytes = 16384;  // 128 rows x 128 bytes: 64 columns of one 16-bit tile
-constexpr int kThreads = 352;      // 11 warps
+constexpr int kThreads = 384;      // 12 warps: two softmax warpgroups, one control warpgroup
+// Registers per thread: the launch gives every thread 168 (65,536 / 384, in
+// steps of 8); the control warpgroup (producer, two MMA issuers, one idle warp)
+// gives registers back so that each softmax thread can hold a whole row of S.
+// 128 x 64 + 256 x 216 = 63,488 <= 384 x 168 = 64,512.
+constexpr uint32_t kRegsControl = 64;
+constexpr uint32_t kRegsSoftmax = 216;
+static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * 168, "register split");
 // The two query tiles run half a period apart, so K_j is released by the
 // later tile; a third K stage lets K_{j+2} load while that tile finishes.
 constexpr int kKStages = 3;
 constexpr int kVStages = 2;
+constexpr int kConsumerWarps = 10;  // 8 softmax warps + 2 MMA issuer warps read each item
 
 template <int D>
 struct FwdSmem {
@@ -56,21 +64,27 @@ struct FwdSmem {
   static constexpr int kK = kQ + 2 * kTile;  // K ring, kKStages
   static constexpr int kV = kK + kKStages * kTile;  // V ring, kVStages
   static constexpr int kBar = kV + kVStages * kTile;
-  static constexpr int kBytes = kBar + 256;
+  static constexpr int kMisc = kBar + 256;   // scheduler response and item slots
+  static constexpr int kBytes = kMisc + 64;
   static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
 };
 
 enum Bars {
-  BQ = 0,
-  BKFULL = 1,    // +stage (3)
-  BKEMPTY = 4,   // +stage (3), one arrival per MMA issuer
-  BVFULL = 7,    // +stage (2)
-  BVEMPTY = 9,   // +stage (2), one arrival per MMA issuer
-  BSFULL = 11,   // +tile
-  BPFULL = 13,   // +tile
-  BODONE = 15,   // +tile
-  BFINAL = 17,   // +tile
-  NBARS = 19
+  BQFULL = 0,    // +tile
+  BQEMPTY = 2,   // +tile: the tile's last S MMA of an item has completed
+  BKFULL = 4,    // +stage (3)
+  BKEMPTY = 7,   // +stage (3), one arrival per MMA issuer
+  BVFULL = 10,   // +stage (2)
+  BVEMPTY = 12,  // +stage (2), one arrival per MMA issuer
+  BSFULL = 14,   // +tile
+  BPFULL = 16,   // +tile
+  BODONE = 18,   // +tile
+  BFINAL = 20,   // +tile
+  BITEMFULL = 22,   // +slot (2): next work item published
+  BITEMEMPTY = 24,  // +slot (2): read by every consumer warp
+  BCLC = 26,        // scheduler response landed
+  BTOKEN = 27,      // +tile: the softmax turn handed to tile X (4 arrivals)
+  NBARS = 29
 };
 
 template <bool BF16>
@@ -93,6 +107,35 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
+// One work item: a pair of 128-row query tiles (A = 2p, B = 2p + 1) of one head.
+struct FwdItem {
+  int bh, kvh, tA, tB, nA, nB, nKV;
+};
+
+__device__ __forceinline__ FwdItem decode_item(int item, int heads, int head_group, int Hq,
+                                               int Hkv, int T, int causal) {
+  const int pairs = (T + 1) / 2;
+  // Groups of heads whose K and V stay in L2; heaviest causal pairs first.
+  const WorkItem wi = grouped_heavy_first(item, heads, pairs, head_group);
+  const int pair = pairs - 1 - wi.rank;
+  FwdItem it;
+  it.bh = wi.head;  // b * Hq + h
+  const int h = it.bh % Hq;
+  const int b = it.bh / Hq;
+  it.kvh = b * Hkv + h / (Hq / Hkv);
+  it.tA = 2 * pair;
+  it.tB = 2 * pair + 1;
+  const bool hasB = it.tB < T;
+  it.nA = causal ? it.tA + 1 : T;
+  it.nB = hasB ? (causal ? it.tB + 1 : T) : 0;
+  it.nKV = it.nA > it.nB ? it.nA : it.nB;
+  return it;
+}
+
+// Persistent over work items: the grid has one CTA per item, and a running CTA
+// takes over the items of CTAs that have not started yet (cluster launch
+// control), so one CTA runs many items back to back and the next item's Q
+// loads and first S MMA overlap the current item's last softmax and epilogue.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -107,29 +150,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::kBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  void* clc_resp = smem + L::kMisc;                                   // 16 bytes
+  volatile int* item_slot = reinterpret_cast<volatile int*>(smem + L::kMisc + 16);  // 2 ints
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int T = (N + kBM - 1) / kBM;
-  const int pairs = (T + 1) / 2;
-  // Groups of heads whose K and V stay in L2; heaviest causal pairs first.
-  const WorkItem wi = grouped_heavy_first(blockIdx.x, heads, pairs, head_group);
-  const int pair = pairs - 1 - wi.rank;
-  const int bh = wi.head;  // b * Hq + h
-  const int h = bh % Hq;
-  const int b = bh / Hq;
-  const int kvh = b * Hkv + h / (Hq / Hkv);
-  const int tA = 2 * pair, tB = 2 * pair + 1;
-  const bool hasB = tB < T;
-  const int nA = causal ? tA + 1 : T;
-  const int nB = hasB ? (causal ? tB + 1 : T) : 0;
-  const int nKV = nA > nB ? nA : nB;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NBARS; ++i) {
       uint32_t cnt = 1;
-      if (i == BPFULL || i == BPFULL + 1) cnt = 4;
+      if (i == BPFULL || i == BPFULL + 1 || i == BTOKEN || i == BTOKEN + 1) cnt = 4;
       if ((i >= BKEMPTY && i < BKEMPTY + kKStages) || (i >= BVEMPTY && i < BVEMPTY + kVStages)) cnt = 2;
+      if (i == BITEMEMPTY || i == BITEMEMPTY + 1) cnt = kConsumerWarps;
       mbar_init(&bar[i], cnt);
     }
     *abort_flag = (*reinterpret_cast<volatile int*>(err) != kDevErrNone) ? 1 : 0;
@@ -144,6 +177,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const bool run = (*abort_flag == 0);
 
+  // Every role walks the same item sequence, published by the producer one
+  // item at a time through a two-slot ring; -1 ends it.  Returns false on abort.
+  auto next_item = [&](int count, int& item) -> bool {
+    const int slot = count & 1;
+    if (!mbar_wait(&bar[BITEMFULL + slot], (count >> 1) & 1, abort_flag, err)) return false;
+    item = item_slot[slot];
+    return true;
+  };
+
+  if (warp >= 8) {
+  // Control warpgroup.  Register reallocation sits inside each role's branch so
+  // that no softmax code is reachable under the control warpgroup's limit.
+  setmaxnreg_dec<kRegsControl>();
   if (run && warp == 8) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -152,39 +198,77 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_v);
       const uint64_t pol_q = l2_policy_evict_first();
       const uint64_t pol_kv = l2_policy_evict_last();
-      mbar_expect_tx(&bar[BQ], L::kTile * (hasB ? 2 : 1));
-      for (int a = 0; a < kAtoms; ++a) {
-        tma_load_3d(smem + L::kQ + a * kAtomBytes, &tm_q, &bar[BQ], a * 64, tA * kBM, bh, pol_q);
-        if (hasB)
-          tma_load_3d(smem + L::kQ + L::kTile + a * kAtomBytes, &tm_q, &bar[BQ], a * 64, tB * kBM,
-                      bh, pol_q);
-      }
-      int kissued = 0, vissued = 0;
-      for (int j = 0; j < nKV; ++j) {
-        const int sk = j % kKStages;
-        const uint32_t pk = (j / kKStages) & 1;
-        const int sv = j % kVStages;
-        const uint32_t pv = (j / kVStages) & 1;
-        if (!mbar_wait(&bar[BKEMPTY + sk], pk ^ 1, abort_flag, err)) break;
-        mbar_expect_tx(&bar[BKFULL + sk], L::kTile);
-        for (int a = 0; a < kAtoms; ++a)
-          tma_load_3d(smem + L::kK + sk * L::kTile + a * kAtomBytes, &tm_k, &bar[BKFULL + sk],
-                      a * 64, j * kBN, kvh, pol_kv);
-        kissued = j + 1;
-        if (!mbar_wait(&bar[BVEMPTY + sv], pv ^ 1, abort_flag, err)) break;
-        mbar_expect_tx(&bar[BVFULL + sv], L::kTile);
-        for (int a = 0; a < kAtoms; ++a)
-          tma_load_3d(smem + L::kV + sv * L::kTile + a * kAtomBytes, &tm_v, &bar[BVFULL + sv],
-                      a * 64, j * kBN, kvh, pol_kv);
-        vissued = j + 1;
+      int item = blockIdx.x;
+      int kv = 0;                  // key tiles loaded so far, over all items (ring position)
+      int kdone = 0, vdone = 0;    // K and V loads issued (differ only after an abort)
+      int quse[2] = {0, 0};        // items so far that used query buffer X
+      int qpend[2] = {-1, -1};     // parity of the last Q load per buffer, -1 if none
+      bool clc_pending = false;    // a scheduler request is in flight
+      bool clc_open = true;        // no request has failed yet
+      int clc_count = 0;
+      bool ok = true;
+      for (int count = 0; ok; ++count) {
+        const int slot = count & 1;
+        if (!(ok = mbar_wait(&bar[BITEMEMPTY + slot], ((count >> 1) & 1) ^ 1, abort_flag, err))) break;
+        item_slot[slot] = item;
+        mbar_arrive(&bar[BITEMFULL + slot]);  // release: the slot write is visible to waiters
+        if (item < 0) break;
+        const FwdItem it = decode_item(item, heads, head_group, Hq, Hkv, T, causal);
+        // Query tiles: buffer X is free once the previous item's last S_X has completed.
+        for (int X = 0; X < 2 && ok; ++X) {
+          const int nX = X ? it.nB : it.nA;
+          if (nX == 0) continue;
+          if (quse[X] > 0 && !(ok = mbar_wait(&bar[BQEMPTY + X], (quse[X] - 1) & 1, abort_flag, err)))
+            break;
+          mbar_expect_tx(&bar[BQFULL + X], L::kTile);
+          for (int a = 0; a < kAtoms; ++a)
+            tma_load_3d(smem + L::kQ + X * L::kTile + a * kAtomBytes, &tm_q, &bar[BQFULL + X],
+                        a * 64, (X ? it.tB : it.tA) * kBM, it.bh, pol_q);
+          qpend[X] = quse[X] & 1;
+          ++quse[X];
+        }
+        for (int j = 0; ok && j < it.nKV; ++j, ++kv) {
+          const int sk = kv % kKStages;
+          const int sv = kv % kVStages;
+          if (!(ok = mbar_wait(&bar[BKEMPTY + sk], ((kv / kKStages) & 1) ^ 1, abort_flag, err))) break;
+          mbar_expect_tx(&bar[BKFULL + sk], L::kTile);
+          for (int a = 0; a < kAtoms; ++a)
+            tma_load_3d(smem + L::kK + sk * L::kTile + a * kAtomBytes, &tm_k, &bar[BKFULL + sk],
+                        a * 64, j * kBN, it.kvh, pol_kv);
+          kdone = kv + 1;
+          if (!(ok = mbar_wait(&bar[BVEMPTY + sv], ((kv / kVStages) & 1) ^ 1, abort_flag, err))) break;
+          mbar_expect_tx(&bar[BVFULL + sv], L::kTile);
+          for (int a = 0; a < kAtoms; ++a)
+            tma_load_3d(smem + L::kV + sv * L::kTile + a * kAtomBytes, &tm_v, &bar[BVFULL + sv],
+                        a * 64, j * kBN, it.kvh, pol_kv);
+          vdone = kv + 1;
+        }
+        if (!ok) break;
+        // Claim the next item only now that this one's loads are all issued, so
+        // that a claimed item waits as little as possible behind this one.
+        int next = -1;
+        if (clc_open) {
+          mbar_expect_tx(&bar[BCLC], 16);
+          clc_try_cancel(clc_resp, &bar[BCLC]);
+          clc_pending = true;
+          if (!(ok = mbar_wait(&bar[BCLC], clc_count & 1, abort_flag, err))) break;
+          clc_pending = false;
+          ++clc_count;
+          next = clc_cancelled_block_x(clc_resp);
+          if (next >= static_cast<int>(gridDim.x)) next = -1;
+          if (next < 0) clc_open = false;
+        }
+        item = next;
       }
       if (*abort_flag) {
         // Let every copy already issued land before shared memory is released.
-        drain_wait(&bar[BQ], 0);
-        for (int j = (kissued > kKStages ? kissued - kKStages : 0); j < kissued; ++j)
-          drain_wait(&bar[BKFULL + j % kKStages], (j / kKStages) & 1);
-        for (int j = (vissued > kVStages ? vissued - kVStages : 0); j < vissued; ++j)
-          drain_wait(&bar[BVFULL + j % kVStages], (j / kVStages) & 1);
+        for (int X = 0; X < 2; ++X)
+          if (qpend[X] >= 0) drain_wait(&bar[BQFULL + X], static_cast<uint32_t>(qpend[X]));
+        for (int u = (kdone > kKStages ? kdone - kKStages : 0); u < kdone; ++u)
+          drain_wait(&bar[BKFULL + u % kKStages], (u / kKStages) & 1);
+        for (int u = (vdone > kVStages ? vdone - kVStages : 0); u < vdone; ++u)
+          drain_wait(&bar[BVFULL + u % kVStages], (u / kVStages) & 1);
+        if (clc_pending) drain_wait(&bar[BCLC], clc_count & 1);
       }
     }
   } else if (run && (warp == 9 || warp == 10)) {
@@ -196,223 +280,294 @@ __global__ void __launch_bounds__(kThreads, 1)
     // issued once PV(j) has completed (tcgen05 orders MMAs only for the same
     // accumulator).  K_j and V_j are released when both tiles are done with
     // them: the empty barriers count one arrival per issuer.
+    const int X = warp - 9;
+    constexpr uint32_t kIdS = idesc_f16(kBM, kBN, BF16, false, false);
+    constexpr uint32_t kIdO = idesc_f16(kBM, D, BF16, false, true);
+    const uint32_t qa = smem_u32(smem + L::kQ) + X * L::kTile;
+    const uint32_t sk = smem_u32(smem + L::kK);
+    const uint32_t sv = smem_u32(smem + L::kV);
+    const uint32_t tS = tmem + X * 128;
+    const uint32_t tO = tmem + 256 + X * 128;
+
+    auto issue_s = [&](int stk) {  // S_X = Q_X K_j^T
+      const uint32_t ka = sk + stk * L::kTile;
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        const uint32_t off = (ks >> 2) * kAtomBytes + (ks & 3) * 32;
+        mma_ss(tS, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), kIdS, ks > 0);
+      }
+      mma_commit(&bar[BSFULL + X]);
+      mma_commit(&bar[BKEMPTY + stk]);
+    };
+    auto issue_pv = [&](int stv, bool first) {
+      const uint32_t va = sv + stv * L::kTile;
+#pragma unroll
+      for (int ks = 0; ks < kBN / 16; ++ks)
+        mma_ts(tO, tS + ks * 8, sdesc_sw128(va + ks * 2048, kAtomBytes, 1024), kIdO,
+               (!first || ks > 0) ? 1u : 0u);
+      mma_commit(&bar[BODONE + X]);
+      mma_commit(&bar[BVEMPTY + stv]);
+    };
+
+    int kv = 0;     // key tiles consumed so far over all items (ring position)
+    int xs = 0;     // S/softmax/PV rounds of this tile so far over all items
+    int quse = 0;   // items so far in which this tile existed
+    bool ok = true;
+    for (int count = 0; ok; ++count) {
+      int item = -1;
+      bool got = true;
+      if (lane == 0) got = next_item(count, item);
+      ok = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
+      item = __shfl_sync(0xffffffffu, item, 0);
+      if (!ok) break;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar[BITEMEMPTY + (count & 1)]);
+      if (item < 0) break;
+      if (lane == 0) {
+        const FwdItem it = decode_item(item, heads, head_group, Hq, Hkv, T, causal);
+        const int nX = X ? it.nB : it.nA;
+        if (nX > 0) {
+          const int stk0 = kv % kKStages;
+          ok = mbar_wait(&bar[BQFULL + X], quse & 1, abort_flag, err) &&
+               mbar_wait(&bar[BKFULL + stk0], (kv / kKStages) & 1, abort_flag, err);
+          // The previous item's last PV reads P from the S columns.
+          if (ok && xs > 0) ok = mbar_wait(&bar[BODONE + X], (xs - 1) & 1, abort_flag, err);
+          if (ok) {
+            tc_fence_after();
+            issue_s(stk0);
+            if (nX == 1) mma_commit(&bar[BQEMPTY + X]);
+          }
+          for (int j = 0; ok && j < nX; ++j) {
+            const int u = kv + j;
+            const int stv = u % kVStages;
+            if (!(ok = mbar_wait(&bar[BVFULL + stv], (u / kVStages) & 1, abort_flag, err))) break;
+            if (!(ok = mbar_wait(&bar[BPFULL + X], (xs + j) & 1, abort_flag, err))) break;
+            tc_fence_after();
+            issue_pv(stv, j == 0);
+            if (j + 1 < nX) {
+              const int stk1 = (u + 1) % kKStages;
+              if (!(ok = mbar_wait(&bar[BKFULL + stk1], ((u + 1) / kKStages) & 1, abort_flag, err))) break;
+              if (!(ok = mbar_wait(&bar[BODONE + X], (xs + j) & 1, abort_flag, err))) break;
+              tc_fence_after();
+              issue_s(stk1);
+              if (j + 2 == nX) mma_commit(&bar[BQEMPTY + X]);  // last S of the item: Q_X free after it
+            }
+          }
+          xs += nX;
+          ++quse;
+        }
+        // Key tiles this query tile does not visit still need this issuer's
+        // release.  It consumes them like the others -- waits until the tile
+        // has landed, then releases it -- so that its view of each ring stays
+        // in step: every wait on a full barrier is then for the phase right
+        // after the last one it observed, which a parity wait can tell apart.
+        for (int j = nX; ok && j < it.nKV; ++j) {
+          const int u = kv + j;
+          const int stk = u % kKStages;
+          const int stv = u % kVStages;
+          if (!(ok = mbar_wait(&bar[BKFULL + stk], (u / kKStages) & 1, abort_flag, err))) break;
+          if (!(ok = mbar_wait(&bar[BVFULL + stv], (u / kVStages) & 1, abort_flag, err))) break;
+          mbar_arrive(&bar[BKEMPTY + stk]);
+          mbar_arrive(&bar[BVEMPTY + stv]);
+        }
+        kv += it.nKV;
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    }
     if (lane == 0) {
-      const int X = warp - 9;
-      const int nX = X ? nB : nA;
-      constexpr uint32_t kIdS = idesc_f16(kBM, kBN, BF16, false, false);
-      constexpr uint32_t kIdO = idesc_f16(kBM, D, BF16, false, true);
-      const uint32_t qa = smem_u32(smem + L::kQ) + X * L::kTile;
-      const uint32_t sk = smem_u32(smem + L::kK);
-      const uint32_t sv = smem_u32(smem + L::kV);
-      const uint32_t tS = tmem + X * 128;
-      const uint32_t tO = tmem + 256 + X * 128;
-
-      auto issue_s = [&](int stk) {  // S_X = Q_X K_j^T
-        const uint32_t ka = sk + stk * L::kTile;
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * kAtomBytes + (ks & 3) * 32;
-          mma_ss(tS, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), kIdS,
-                 ks > 0);
-        }
-        mma_commit(&bar[BSFULL + X]);
-        mma_commit(&bar[BKEMPTY + stk]);
-      };
-      auto issue_pv = [&](int stv, int j) {
-        const uint32_t va = sv + stv * L::kTile;
-#pragma unroll
-        for (int ks = 0; ks < kBN / 16; ++ks)
-          mma_ts(tO, tS + ks * 8, sdesc_sw128(va + ks * 2048, kAtomBytes, 1024), kIdO,
-                 (j > 0 || ks > 0) ? 1u : 0u);
-        mma_commit(&bar[BODONE + X]);
-        mma_commit(&bar[BVEMPTY + stv]);
-      };
-
-      bool ok = true;
-      if (nX > 0) {
-        ok = mbar_wait(&bar[BQ], 0, abort_flag, err) && mbar_wait(&bar[BKFULL], 0, abort_flag, err);
-        if (ok) {
-          tc_fence_after();
-          issue_s(0);
-        }
-      }
-      for (int j = 0; ok && j < nX; ++j) {
-        const int stv = j % kVStages;
-        if (!(ok = mbar_wait(&bar[BVFULL + stv], (j / kVStages) & 1, abort_flag, err))) break;
-        if (!(ok = mbar_wait(&bar[BPFULL + X], j & 1, abort_flag, err))) break;
-        tc_fence_after();
-        issue_pv(stv, j);
-        if (j + 1 < nX) {
-          const int stk1 = (j + 1) % kKStages;
-          if (!(ok = mbar_wait(&bar[BKFULL + stk1], ((j + 1) / kKStages) & 1, abort_flag, err))) break;
-          if (!(ok = mbar_wait(&bar[BODONE + X], j & 1, abort_flag, err))) break;
-          tc_fence_after();
-          issue_s(stk1);
-        }
-      }
-      // Key tiles this query tile does not visit still need this issuer's
-      // release.  Its arrival for a use of a stage may only come after that
-      // stage's previous use has been released by both issuers.
-      for (int j = nX; ok && j < nKV; ++j) {
-        const int stk = j % kKStages;
-        const int stv = j % kVStages;
-        if (j >= kKStages && !(ok = mbar_wait(&bar[BKEMPTY + stk], ((j / kKStages) - 1) & 1,
-                                              abort_flag, err)))
-          break;
-        if (j >= kVStages && !(ok = mbar_wait(&bar[BVEMPTY + stv], ((j / kVStages) - 1) & 1,
-                                              abort_flag, err)))
-          break;
-        mbar_arrive(&bar[BKEMPTY + stk]);
-        mbar_arrive(&bar[BVEMPTY + stv]);
-      }
       // Every MMA this thread issued has completed before TMEM is released.
       mma_commit(&bar[BFINAL + X]);
       drain_wait(&bar[BFINAL + X], 0);
     }
-  } else if (run && warp < 8) {
-    // ------------------------------------------------------------ softmax
+  }
+  } else {
+  setmaxnreg_inc<kRegsSoftmax>();
+  if (run) {
+    // ------------------------------------------------------------ softmax + epilogue
     const int X = warp >> 2;
-    const int t = X ? tB : tA;
-    const int nX = X ? nB : nA;
     const int r = threadIdx.x & 127;
-    const int q = t * kBM + r;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_off + X * 128;
     const uint32_t tO = tmem + lane_off + 256 + X * 128;
-    float m_run = -INFINITY;
-    float l_run = 0.f;
     const bool pos_scale = scale_log2 > 0.f;
     const float sfac = pos_scale ? scale_log2 : 1.0f;
+    int xs = 0;           // softmax rounds of this tile so far over all items
+    int tokens = 0;       // turns handed to this tile so far
+    int prev_nA = 0, prev_nB = 0;  // rounds of each tile in the previous item (0: none yet)
     bool ok = true;
-    for (int j = 0; j < nX; ++j) {
-      // The two tiles' softmaxes take turns -- A(0), B(0), A(1), B(1), ... -- so
-      // each runs alone on the SM's ALUs while the tensor core works on the
-      // other tile.  A(j) follows B(j-1); B(j) follows A(j) where tile A has one.
-      bool turn = true;
-      if (X == 0 && j > 0 && nB > 0) turn = mbar_wait(&bar[BPFULL + 1], (j - 1) & 1, abort_flag, err);
-      if (X == 1 && j < nA) turn = mbar_wait(&bar[BPFULL], j & 1, abort_flag, err);
-      ok = __all_sync(0xffffffffu, turn && mbar_wait(&bar[BSFULL + X], j & 1, abort_flag, err));
+    for (int count = 0; ok; ++count) {
+      int item = -1;
+      bool got = true;
+      if (lane == 0) got = next_item(count, item);
+      ok = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
+      item = __shfl_sync(0xffffffffu, item, 0);
       if (!ok) break;
-      tc_fence_after();
-      // x holds the scores as raw bits: s * scale * log2(e) after the first pass.
-      uint32_t x[kBN];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar[BITEMEMPTY + (count & 1)]);
+      if (item < 0) break;
+      const FwdItem it = decode_item(item, heads, head_group, Hq, Hkv, T, causal);
+      const int t = X ? it.tB : it.tA;
+      const int nX = X ? it.nB : it.nA;
+      const int m = it.nA < it.nB ? it.nA : it.nB;  // rounds both tiles have
+      const int q = t * kBM + r;
+      float m_run = -INFINITY;
+      float l_run = 0.f;
+      for (int j = 0; j < nX; ++j) {
+        // The two tiles' softmaxes take turns, so that each runs alone on the
+        // SM's ALUs while the tensor core works on the other tile.  Over all
+        // items the rounds run in one sequence: per item A(0), B(0), A(1),
+        // B(1), ..., then the rounds only one tile has (B's last round under
+        // causal masking; every round of A when the item has no tile B).  A
+        // tile waits for the turn where the round before its own in that
+        // sequence is the other tile's, and hands the turn over where the
+        // round after its own is the other tile's.  Every item starts with
+        // A(0).  Hand-overs to one tile alternate with hand-overs back, so
+        // each wait is for the phase right after the last one this tile saw.
+        bool wait_turn, pass_turn;
+        if (X == 0) {
+          wait_turn = (j == 0) ? (prev_nA > 0 && prev_nB >= prev_nA) : (j <= m);
+          pass_turn = j < m;
+        } else {
+          wait_turn = j < m;
+          pass_turn = (j < m - 1) || (j == m - 1 && it.nA >= it.nB) || (j >= m && j == it.nB - 1);
+        }
+        bool turn = true;
+        if (wait_turn) {
+          turn = mbar_wait(&bar[BTOKEN + X], tokens & 1, abort_flag, err);
+          ++tokens;
+        }
+        ok = __all_sync(0xffffffffu, turn && mbar_wait(&bar[BSFULL + X], (xs + j) & 1, abort_flag, err));
+        if (!ok) break;
+        tc_fence_after();
+        // x holds the scores as raw bits: s * scale * log2(e) after the first pass.
+        uint32_t x[kBN];
 #pragma unroll
-      for (int c = 0; c < kBN; c += 32) tmem_ld32(tS + c, x + c);
-      tmem_ld_wait();
-      reg_fence<kBN>(x);
-      const int kbase = j * kBN;
-      const bool diag = causal && (j == t);
-      // Scores stay raw when scale > 0 (the exponent is then one FFMA,
-      // s * scale*log2(e) - m, and the row maximum of raw scores times the
-      // positive factor is the maximum of the scaled scores); for scale <= 0
-      // they are scaled first and the factor below is 1.
-      if (!pos_scale) {
+        for (int c = 0; c < kBN; c += 32) tmem_ld32(tS + c, x + c);
+        tmem_ld_wait();
+        reg_fence<kBN>(x);
+        const int kbase = j * kBN;
+        const bool diag = causal && (j == t);
+        // Scores stay raw when scale > 0 (the exponent is then one FFMA,
+        // s * scale*log2(e) - m, and the row maximum of raw scores times the
+        // positive factor is the maximum of the scaled scores); for scale <= 0
+        // they are scaled first and the factor below is 1.
+        if (!pos_scale) {
 #pragma unroll
-        for (int c = 0; c < kBN; ++c) x[c] = __float_as_uint(__uint_as_float(x[c]) * scale_log2);
-      }
-      if (diag || kbase + kBN > N) {
-        int lim = N - kbase;
-        if (diag && r + 1 < lim) lim = r + 1;  // key kbase + c visible iff c <= r
+          for (int c = 0; c < kBN; ++c) x[c] = __float_as_uint(__uint_as_float(x[c]) * scale_log2);
+        }
+        if (diag || kbase + kBN > N) {
+          int lim = N - kbase;
+          if (diag && r + 1 < lim) lim = r + 1;  // key kbase + c visible iff c <= r
 #pragma unroll
-        for (int c = 0; c < kBN; ++c)
-          if (c >= lim) x[c] = __float_as_uint(-INFINITY);
-      }
-      // row maximum as eight independent chains, then a tree
-      // eight chains (chain u: scores u, u+8, ..., u+120) of three-input maxima
-      float m8[8];
+          for (int c = 0; c < kBN; ++c)
+            if (c >= lim) x[c] = __float_as_uint(-INFINITY);
+        }
+        // row maximum: eight independent chains (chain u: scores u, u+8, ...,
+        // u+120) of three-input maxima, then a tree
+        float m8[8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        float m = fmax3(__uint_as_float(x[u]), __uint_as_float(x[u + 8]), __uint_as_float(x[u + 16]));
+        for (int u = 0; u < 8; ++u) {
+          float m = fmax3(__uint_as_float(x[u]), __uint_as_float(x[u + 8]), __uint_as_float(x[u + 16]));
 #pragma unroll
-        for (int k = 3; k < 15; k += 2)
-          m = fmax3(m, __uint_as_float(x[u + 8 * k]), __uint_as_float(x[u + 8 * k + 8]));
-        m8[u] = fmaxf(m, __uint_as_float(x[u + 120]));
-      }
-      const float mx =
-          fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7])) * sfac;
-      // Conditional rescale: keep the stale maximum unless it grew by more than 8
-      // (p <= 2^8 then); the decision is warp-uniform because TMEM access is.
-      float alpha = 1.0f;
-      bool rescale = false;
-      if (j == 0) {
-        m_run = mx;
-      } else {
-        const bool need = mx > m_run + 8.0f;
-        rescale = __any_sync(0xffffffffu, need);
-        if (need) {
-          alpha = ex2_approx(m_run - mx);
+          for (int k = 3; k < 15; k += 2)
+            m = fmax3(m, __uint_as_float(x[u + 8 * k]), __uint_as_float(x[u + 8 * k + 8]));
+          m8[u] = fmaxf(m, __uint_as_float(x[u + 120]));
+        }
+        const float mx =
+            fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7])) * sfac;
+        // Conditional rescale: keep the stale maximum unless it grew by more than 8
+        // (p <= 2^8 then); the decision is warp-uniform because TMEM access is.
+        float alpha = 1.0f;
+        bool rescale = false;
+        if (j == 0) {
           m_run = mx;
+        } else {
+          const bool need = mx > m_run + 8.0f;
+          rescale = __any_sync(0xffffffffu, need);
+          if (need) {
+            alpha = ex2_approx(m_run - mx);
+            m_run = mx;
+          }
+        }
+        // exponent arguments and row sums two at a time (packed fp32)
+        const uint64_t sfac2 = f2_pack(sfac, sfac);
+        const uint64_t negm2 = f2_pack(-m_run, -m_run);
+        uint64_t rs2[2] = {0ull, 0ull};
+#pragma unroll
+        for (int c = 0; c < kBN; c += 32) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            float a0, a1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(x[c + 2 * e]), __uint_as_float(x[c + 2 * e + 1])),
+                             sfac2, negm2),
+                      a0, a1);
+            const float p0 = ex2_approx(a0);
+            const float p1 = ex2_approx(a1);
+            rs2[e & 1] = f2_add(rs2[e & 1], f2_pack(p0, p1));
+            pk[e] = pack2<BF16>(p0, p1);
+          }
+          tmem_st16(tS + c / 2, pk);
+        }
+        float r0, r1, r2, r3;
+        f2_unpack(rs2[0], r0, r1);
+        f2_unpack(rs2[1], r2, r3);
+        l_run = l_run * alpha + ((r0 + r1) + (r2 + r3));
+        if (rescale) {
+          // O_X was last written by PV_X(j-1), which completed before S_X(j) was issued.
+#pragma unroll
+          for (int c = 0; c < D; c += 32) {
+            uint32_t o[32];
+            tmem_ld32(tO + c, o);
+            tmem_ld_wait();
+            reg_fence<32>(o);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st32(tO + c, o);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&bar[BPFULL + X]);
+          if (pass_turn) mbar_arrive(&bar[BTOKEN + (X ^ 1)]);
         }
       }
-      // exponent arguments and row sums two at a time (packed fp32)
-      const uint64_t sfac2 = f2_pack(sfac, sfac);
-      const uint64_t negm2 = f2_pack(-m_run, -m_run);
-      uint64_t rs2[2] = {0ull, 0ull};
-#pragma unroll
-      for (int c = 0; c < kBN; c += 32) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          float a0, a1;
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(x[c + 2 * e]), __uint_as_float(x[c + 2 * e + 1])),
-                           sfac2, negm2),
-                    a0, a1);
-          const float p0 = ex2_approx(a0);
-          const float p1 = ex2_approx(a1);
-          rs2[e & 1] = f2_add(rs2[e & 1], f2_pack(p0, p1));
-          pk[e] = pack2<BF16>(p0, p1);
-        }
-        tmem_st16(tS + c / 2, pk);
-      }
-      float r0, r1, r2, r3;
-      f2_unpack(rs2[0], r0, r1);
-      f2_unpack(rs2[1], r2, r3);
-      l_run = l_run * alpha + ((r0 + r1) + (r2 + r3));
-      if (rescale) {
-        // O_X was last written by PV_X(j-1), which completed before S_X(j) was issued.
+      if (ok && nX > 0)
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar[BODONE + X], (xs + nX - 1) & 1, abort_flag, err));
+      if (ok && nX > 0) {
+        // Epilogue.  The next item's first PV overwrites O_X; it is issued only
+        // after this warp's next P arrival, which follows these loads.
+        tc_fence_after();
+        const float inv_l = 1.0f / l_run;
+        const bool valid = q < N;
+        uint16_t* orow = reinterpret_cast<uint16_t*>(out) + (static_cast<size_t>(it.bh) * N + q) * D;
 #pragma unroll
         for (int c = 0; c < D; c += 32) {
           uint32_t o[32];
           tmem_ld32(tO + c, o);
           tmem_ld_wait();
           reg_fence<32>(o);
+          uint32_t pk[16];
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st32(tO + c, o);
+          for (int e = 0; e < 16; ++e)
+            pk[e] = pack2<BF16>(__uint_as_float(o[2 * e]) * inv_l, __uint_as_float(o[2 * e + 1]) * inv_l);
+          if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c);
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4)
+              dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+          }
         }
+        if (valid)
+          lse_out[static_cast<size_t>(it.bh) * N + q] = (m_run + log2f(l_run)) * 0.69314718055994530942f;
       }
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar[BPFULL + X]);
+      xs += nX;
+      prev_nA = it.nA;
+      prev_nB = it.nB;
     }
-    if (ok && nX > 0) ok = __all_sync(0xffffffffu, mbar_wait(&bar[BODONE + X], (nX - 1) & 1,
-                                                             abort_flag, err));
-    if (ok && nX > 0) {
-      tc_fence_after();
-      const float inv_l = 1.0f / l_run;
-      const bool valid = q < N;
-      uint16_t* orow = reinterpret_cast<uint16_t*>(out) + (static_cast<size_t>(bh) * N + q) * D;
-#pragma unroll
-      for (int c = 0; c < D; c += 32) {
-        uint32_t o[32];
-        tmem_ld32(tO + c, o);
-        tmem_ld_wait();
-        reg_fence<32>(o);
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e)
-          pk[e] = pack2<BF16>(__uint_as_float(o[2 * e]) * inv_l, __uint_as_float(o[2 * e + 1]) * inv_l);
-        if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c);
-#pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4)
-            dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
-        }
-      }
-      if (valid)
-        lse_out[static_cast<size_t>(bh) * N + q] = (m_run + log2f(l_run)) * 0.69314718055994530942f;
-    }
+  }
   }
 
   tc_fence_before();

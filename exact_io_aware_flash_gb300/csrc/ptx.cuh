@@ -154,6 +154,53 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   return p;
 }
 
+// ---------------------------------------------------------------- cluster launch control
+// Work stealing through the hardware block scheduler (sm_100-class GPUs): a
+// running CTA asks to cancel the launch of a CTA that has not started yet and,
+// if that succeeds, does the cancelled CTA's work itself.  Every block index
+// is then processed exactly once -- by its own CTA or by the one that
+// cancelled it -- and no counter in global memory is needed.  The 16-byte
+// response lands in shared memory at `resp` (16-byte aligned) and completes
+// 16 transaction bytes on `bar`; the caller arms `bar` with expect_tx(16).
+// After a request that fails (nothing left to cancel) no further request may
+// be made, and at most one request is outstanding at a time.
+__device__ __forceinline__ void clc_try_cancel(void* resp, uint64_t* bar) {
+  asm volatile(
+      "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128"
+      " [%0], [%1];" ::"r"(smem_u32(resp)),
+      "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Decodes a completed response: returns the cancelled CTA's blockIdx.x, or -1
+// if the request failed.
+__device__ __forceinline__ int clc_cancelled_block_x(const void* resp) {
+  uint32_t ok, x;
+  asm volatile(
+      "{\n .reg .b128 r;\n .reg .pred p;\n ld.shared.b128 r, [%2];\n"
+      " clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n"
+      " selp.u32 %0, 1, 0, p;\n"
+      " clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, r;\n}\n"
+      : "=r"(ok), "=r"(x)
+      : "r"(smem_u32(resp))
+      : "memory");
+  return ok ? static_cast<int>(x) : -1;
+}
+
+// ---------------------------------------------------------------- register reallocation
+// Moves registers between warpgroups of one CTA (all four warps of a
+// warpgroup execute the same instruction).  The increase waits until the pool
+// the CTA was launched with (threads x registers per thread at launch) has
+// room, so the warpgroups' shares must add up to at most that total.
+template <uint32_t R>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(R));
+}
+template <uint32_t R>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(R));
+}
+
 // Named barrier over `nthreads` threads (id 0 is __syncthreads).
 __device__ __forceinline__ void named_barrier(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
