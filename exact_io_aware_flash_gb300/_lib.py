@@ -196,13 +196,13 @@ def backward(q, k, v, o, lse, dO, causal: bool = False, scale: float | None = No
     return dq, dk, dv
 
 
-def set_backward_event_hooks(before_dkdv=None, before_dq=None, after_dq=None) -> None:
-    """Record CUDA events around the backward's dK/dV and dQ kernels (see fa.h).
+def set_backward_event_hooks(before_dq=None, before_dkdv=None, after_dkdv=None) -> None:
+    """Record CUDA events around the backward's dQ and dK/dV kernels (see fa.h).
 
     The arguments are torch.cuda.Event objects that have been recorded at
     least once (so their CUDA handles exist); three Nones stop the hook.
     """
-    evs = (before_dkdv, before_dq, after_dq)
+    evs = (before_dq, before_dkdv, after_dkdv)
     _raise(load().fa_set_backward_event_hooks(*(None if e is None else e.cuda_event for e in evs)))
 
 

@@ -107,14 +107,15 @@ int get_device_state(DeviceState** out) {
   return FA_OK;
 }
 
-// [heads, N, d] 16-bit tensor, box {64, 128, 1}, 128-byte swizzle, zero fill out of bounds.
+// [heads, N, d] 16-bit tensor, box {64, box_rows, 1}, 128-byte swizzle, zero fill out of
+// bounds.  Loads use 128-row boxes; the backward's stores use 32-row boxes (one warp each).
 int encode_tile_map(CUtensorMap* map, const void* base, int heads, int N, int d, int bf16,
-                    const char* name) {
+                    const char* name, int box_rows = 128) {
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
                         static_cast<cuuint64_t>(heads)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
                            static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2};
-  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = g_encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                         3, const_cast<void*>(base), dims, strides, box, estr,
@@ -333,6 +334,10 @@ int fa_backward(const void* q, const void* k, const void* v, const void* o, cons
   if ((rc = encode_tile_map(&a.tm_k, k, B * Hkv, N, d, s.bf16, "k"))) return rc;
   if ((rc = encode_tile_map(&a.tm_v, v, B * Hkv, N, d, s.bf16, "v"))) return rc;
   if ((rc = encode_tile_map(&a.tm_do, dO, B * Hq, N, d, s.bf16, "dO"))) return rc;
+  if ((rc = encode_tile_map(&a.tm_o, o, B * Hq, N, d, s.bf16, "o"))) return rc;
+  if ((rc = encode_tile_map(&a.tm_dq, dq, B * Hq, N, d, s.bf16, "dq", 32))) return rc;
+  if ((rc = encode_tile_map(&a.tm_dk, dk, B * Hkv, N, d, s.bf16, "dk", 32))) return rc;
+  if ((rc = encode_tile_map(&a.tm_dv, dv, B * Hkv, N, d, s.bf16, "dv", 32))) return rc;
   a.o = o;
   a.dO = dO;
   a.lse = lse;
@@ -341,21 +346,21 @@ int fa_backward(const void* q, const void* k, const void* v, const void* o, cons
   a.dk = dk;
   a.dv = dv;
   a.err = st->err_word;
-  a.ev_before_dkdv = t_ev_hooks[0];
-  a.ev_before_dq = t_ev_hooks[1];
-  a.ev_after_dq = t_ev_hooks[2];
+  a.ev_before_dq = t_ev_hooks[0];
+  a.ev_before_dkdv = t_ev_hooks[1];
+  a.ev_after_dkdv = t_ev_hooks[2];
   cudaError_t e = fa::launch_backward(s, a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(FA_ERR_CUDA, "backward launch: %s", cudaGetErrorString(e));
   return FA_OK;
 }
 
-int fa_set_backward_event_hooks(void* before_dkdv, void* before_dq, void* after_dq) {
+int fa_set_backward_event_hooks(void* before_dq, void* before_dkdv, void* after_dkdv) {
   t_last_error.clear();
-  const int n = (before_dkdv != nullptr) + (before_dq != nullptr) + (after_dq != nullptr);
+  const int n = (before_dq != nullptr) + (before_dkdv != nullptr) + (after_dkdv != nullptr);
   if (n != 0 && n != 3) return fail(FA_ERR_INVALID, "pass all three events or none");
-  t_ev_hooks[0] = static_cast<cudaEvent_t>(before_dkdv);
-  t_ev_hooks[1] = static_cast<cudaEvent_t>(before_dq);
-  t_ev_hooks[2] = static_cast<cudaEvent_t>(after_dq);
+  t_ev_hooks[0] = static_cast<cudaEvent_t>(before_dq);
+  t_ev_hooks[1] = static_cast<cudaEvent_t>(before_dkdv);
+  t_ev_hooks[2] = static_cast<cudaEvent_t>(after_dkdv);
   return FA_OK;
 }
 

@@ -8,12 +8,18 @@
 //     P    = exp(scale * Q K^T - LSE)           (recomputed, never stored)
 //     dV   = P^T dO
 //     dP   = dO V^T
-//     D_i  = sum_c dO_ic O_ic                    (preprocessing kernel)
+//     D_i  = sum_c dO_ic O_ic
 //     dS   = P o (dP - D)
 //     dQ   = scale * dS K,   dK = scale * dS^T Q
 //
-// Kernels, all on the caller's stream:
-//   fa_bwd_pre_kernel    D = rowsum(dO o O).
+// Kernels, in launch order on the caller's stream:
+//   fa_bwd_dq_kernel     one CTA per (query head, 128-query tile i), looping over
+//                        key tiles j (causal: j <= i), dQ accumulating in TMEM:
+//                          D_i (rows of O and dO, while the first S is computed)
+//                          S = Q_i K_j^T,  dP = dO_i V_j^T        (SMEM x SMEM)
+//                          P, dS                               (compute warps)
+//                          dQ += dS K_j                        (TMEM A operand)
+//                        It also writes D for the next kernel.
 //   fa_bwd_dkdv_kernel   one CTA per (KV head, 128-key tile j), looping over the
 //                        KV head's query heads and query tiles i (causal: i >= j),
 //                        in the transposed orientation so the key tile owns the
@@ -21,11 +27,8 @@
 //                          S^T  = K_j Q_i^T,  dP^T = V_j dO_i^T   (SMEM x SMEM)
 //                          P^T, dS^T                           (compute warps)
 //                          dV  += P^T dO_i,   dK  += dS^T Q_i     (TMEM A operand)
-//   fa_bwd_dq_kernel     one CTA per (query head, 128-query tile i), looping over
-//                        key tiles j (causal: j <= i), dQ accumulating in TMEM:
-//                          S = Q_i K_j^T,  dP = dO_i V_j^T        (SMEM x SMEM)
-//                          P, dS                               (compute warps)
-//                          dQ += dS K_j                        (TMEM A operand)
+// Outputs leave as 16-bit tiles staged in idle shared memory and written by
+// TMA stores (a thread-per-row global store pattern costs a whole iteration).
 // dQ is therefore summed over key tiles inside one CTA rather than with atomic
 // adds across CTAs (the primer notes the default backward uses atomic adds and
 // is nondeterministic, section "Backward pass: recomputation instead of
@@ -93,62 +96,31 @@ __device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile, int ks) {
   return sdesc_sw128(tile + ks * 2048, kAtomBytes, 1024);
 }
 
-// TMEM row (D fp32 columns at taddr) * mul -> 16-bit row in global memory.
+// TMEM row (D fp32 columns at taddr) * mul -> 16-bit row `row` of a 128-row
+// tile in shared memory, in the layout a 128-byte-swizzled TMA box expects:
+// 64-column atoms of 128 x 128 bytes, 16-byte chunk c of row r at chunk
+// position c ^ (r mod 8).  Eight consecutive rows cover all 32 banks, so a
+// warp's 16-byte stores are conflict-free.
 template <int D, bool BF16>
-__device__ __forceinline__ void store_rows_from_tmem(uint32_t taddr, uint16_t* row, float mul,
-                                                     bool valid) {
+__device__ __forceinline__ void stage_row_from_tmem(uint32_t taddr, uint8_t* tile, int row,
+                                                    float mul) {
 #pragma unroll
-  for (int c = 0; c < D; c += 32) {
-    uint32_t v[32];
+  for (int c = 0; c < D; c += 64) {  // one 64-column atom per TMEM round trip
+    uint32_t v[64];
     tmem_ld32(taddr + c, v);
+    tmem_ld32(taddr + c + 32, v + 32);
     tmem_ld_wait();
-    reg_fence<32>(v);
-    uint32_t pk[16];
+    reg_fence<64>(v);
+    uint8_t* rowp = tile + (c / 64) * kAtomBytes + row * 128;
 #pragma unroll
-    for (int e = 0; e < 16; ++e)
-      pk[e] = pack2<BF16>(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
-    if (valid) {
-      uint4* dst = reinterpret_cast<uint4*>(row + c);
+    for (int ch = 0; ch < 8; ++ch) {  // 16-byte chunk ch: columns c + 8*ch .. +7
+      uint32_t pk[4];
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4)
-        dst[q4] = make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+      for (int e = 0; e < 4; ++e)
+        pk[e] = pack2<BF16>(__uint_as_float(v[8 * ch + 2 * e]) * mul,
+                            __uint_as_float(v[8 * ch + 2 * e + 1]) * mul);
+      *reinterpret_cast<uint4*>(rowp + ((ch ^ (row & 7)) * 16)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
     }
-  }
-}
-
-// ------------------------------------------------------------------ preprocessing
-// D_i = sum_c dO_ic O_ic (fp32).  D/8 threads per row, 16 bytes each.
-template <int D, bool BF16>
-__global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const uint4* __restrict__ O,
-                                                         const uint4* __restrict__ dO,
-                                                         float* __restrict__ Drow, long rows) {
-  constexpr int kTpr = D / 8;  // threads per row
-  const long total = rows * kTpr;
-  const long stride = static_cast<long>(gridDim.x) * blockDim.x;
-  const int lane = threadIdx.x & 31;
-  const int sub = threadIdx.x % kTpr;
-  // Whole warps iterate together so the row reduction's shuffles see all lanes.
-  for (long w0 = static_cast<long>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31); w0 < total;
-       w0 += stride) {
-    const long t = w0 + lane;
-    const bool in = t < total;
-    float acc = 0.f;
-    if (in) {
-      const uint4 a = O[t];
-      const uint4 b = dO[t];
-      const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
-      const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 x = unpack2<BF16>(aw[e]);
-        const float2 y = unpack2<BF16>(bw[e]);
-        acc = fmaf(x.x, y.x, acc);
-        acc = fmaf(x.y, y.y, acc);
-      }
-    }
-#pragma unroll
-    for (int off = kTpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (in && sub == 0) Drow[t / kTpr] = acc;
   }
 }
 
@@ -185,8 +157,8 @@ template <int D, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                       const float* __restrict__ lse, const float* __restrict__ Drow,
-                       void* __restrict__ dk_out, void* __restrict__ dv_out, int heads,
+                       const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
+                       const float* __restrict__ lse, const float* __restrict__ Drow, int heads,
                        int head_group, int Hq, int Hkv, int N, int causal, float scale, int* err) {
   using L = DkdvSmem<D>;
   constexpr int kAtoms = D / 64;
@@ -219,7 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (i == KB_PREADY || i == KB_DSREADY) cnt = 4;
       mbar_init(&bar[i], cnt);
     }
-    *abort_flag = (*reinterpret_cast<volatile int*>(err) != kDevErrNone) ? 1 : 0;
+    *abort_flag = 0;  // the producer checks the error word once its first loads are issued
     fence_mbar_init();
   }
   if (warp == 5) {
@@ -229,9 +201,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const bool run = (*abort_flag == 0);
 
-  if (run && warp == 4) {
+  if (warp == 4) {
     // ------------------------------------------------------------ producer
     float* s_lse = reinterpret_cast<float*>(smem + L::kLse);
     float* s_d = reinterpret_cast<float*>(smem + L::kDrow);
@@ -266,6 +237,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         a * 64, i * kBlk, bhq, pol_q);
           }
           issued = it + 1;
+          // A CTA that starts after another one raised the error word stops at
+          // its next wait; reading the word only now keeps its latency off the
+          // path to the first MMA.
+          if (it == 0 && *reinterpret_cast<volatile int*>(err) != kDevErrNone) *abort_flag = 1;
         }
       }
       if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) == 0) break;  // also orders the stage reuse
@@ -288,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int it = (issued > 2 ? issued - 2 : 0); it < issued; ++it)
         drain_wait(&bar[KB_QFULL + (it & 1)], (it >> 1) & 1);
     }
-  } else if (run && warp == 5) {
+  } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_f16(kBlk, kBlk, BF16, false, false);  // S^T, dP^T
@@ -360,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(&bar[KB_FINAL]);
       drain_wait(&bar[KB_FINAL], 0);
     }
-  } else if (run && warp < 4) {
+  } else if (warp < 4) {
     // ------------------------------------------------------------ compute: P^T, dS^T
     const int t = threadIdx.x;  // key row within the tile
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
@@ -456,17 +431,42 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar[KB_DSREADY]);
     }
-    // dV and dK epilogue
+    // Epilogue: dV and dK leave as 16-bit tiles staged in shared memory and
+    // written by TMA stores.  dV is final once the last dV MMA has completed;
+    // by then every MMA that reads K or V has completed too (they were issued
+    // before it), so dV is staged over K while the last dK MMA still runs,
+    // and dK over V once every MMA is done.
+    const bool store_rows = j * kBlk + 32 * warp < N;  // a store box must start inside the tensor
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bar[KB_DVDONE], (n_it - 1) & 1, abort_flag, err));
+    if (ok) {
+      tc_fence_after();
+      uint8_t* st_dv = smem + L::kK;
+      stage_row_from_tmem<D, BF16>(tmem + lane_off + kColDV, st_dv, t, 1.0f);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0 && store_rows) {
+#pragma unroll
+        for (int a = 0; a < kAtoms; ++a)
+          tma_store_3d(&tm_dv, st_dv + a * kAtomBytes + warp * 4096, a * 64, j * kBlk + 32 * warp, bkv);
+        bulk_commit_group();
+      }
+    }
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bar[KB_FINAL], 0, abort_flag, err));
     if (ok) {
       tc_fence_after();
-      const int kv = j * kBlk + t;
-      const size_t off = (static_cast<size_t>(bkv) * N + kv) * D;
-      store_rows_from_tmem<D, BF16>(tmem + lane_off + kColDV, reinterpret_cast<uint16_t*>(dv_out) + off,
-                                    1.0f, kv < N);
-      store_rows_from_tmem<D, BF16>(tmem + lane_off + kColDK, reinterpret_cast<uint16_t*>(dk_out) + off,
-                                    scale, kv < N);
+      uint8_t* st_dk = smem + L::kV;
+      stage_row_from_tmem<D, BF16>(tmem + lane_off + kColDK, st_dk, t, scale);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0 && store_rows) {
+#pragma unroll
+        for (int a = 0; a < kAtoms; ++a)
+          tma_store_3d(&tm_dk, st_dk + a * kAtomBytes + warp * 4096, a * 64, j * kBlk + 32 * warp, bkv);
+        bulk_commit_group();
+      }
     }
+    // Shared memory stays allocated until every store issued here has read it.
+    if (lane == 0) bulk_wait_read_all();
   }
 
   tc_fence_before();
@@ -509,15 +509,18 @@ enum DqBars {
   QB_DSREADY = 15, // dS written to TMEM (4 warps)
   QB_DQDONE = 16,  // dQ MMA done: dS columns free
   QB_FINAL = 17,
-  QB_N = 18
+  QB_OFREE = 18,   // O_i read (4 warps): K stage 2 may be loaded
+  QB_O = 19,       // O_i landed (in K stage 2)
+  QB_N = 20
 };
 
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                     const float* __restrict__ lse, const float* __restrict__ Drow,
-                     void* __restrict__ dq_out, int heads, int head_group, int Hq, int Hkv, int N,
+                     const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_o,
+                     const float* __restrict__ lse, float* __restrict__ Drow, int heads,
+                     int head_group, int Hq, int Hkv, int N,
                      int causal, float scale, int* err) {
   using L = DqSmem<D>;
   constexpr int kAtoms = D / 64;
@@ -544,10 +547,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int k = 0; k < QB_N; ++k) {
       uint32_t cnt = 1;
-      if (k == QB_SFREE || k == QB_DPFREE || k == QB_DSREADY) cnt = 4;
+      if (k == QB_SFREE || k == QB_DPFREE || k == QB_DSREADY || k == QB_OFREE) cnt = 4;
       mbar_init(&bar[k], cnt);
     }
-    *abort_flag = (*reinterpret_cast<volatile int*>(err) != kDevErrNone) ? 1 : 0;
+    *abort_flag = 0;  // the producer checks the error word once its first loads are issued
     fence_mbar_init();
   }
   if (warp == 5) {
@@ -557,15 +560,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const bool run = (*abort_flag == 0);
 
-  if (run && warp == 4) {
+  if (warp == 4) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       tma_prefetch_desc(&tm_do);
+      tma_prefetch_desc(&tm_o);
       const uint64_t pol_q = l2_policy_evict_first();
       const uint64_t pol_kv = l2_policy_evict_last();
       mbar_expect_tx(&bar[QB_Q], 2 * L::kTile);
@@ -574,11 +577,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(smem + L::kdO + a * kAtomBytes, &tm_do, &bar[QB_Q], a * 64, i * kBlk, bhq, pol_q);
       }
       int kissued = 0, vissued = 0;
+      bool o_issued = false;
       for (int jj = 0; jj < n_j; ++jj) {
         const int sk = jj % kDqKStages;
         const uint32_t pk = (jj / kDqKStages) & 1;
         const int sv = jj & 1;
         const uint32_t pv = (jj >> 1) & 1;
+        if (jj == 2 && !mbar_wait(&bar[QB_OFREE], 0, abort_flag, err)) break;
         if (!mbar_wait(&bar[QB_KEMPTY + sk], pk ^ 1, abort_flag, err)) break;
         mbar_expect_tx(&bar[QB_KFULL + sk], L::kTile);
         for (int a = 0; a < kAtoms; ++a)
@@ -591,16 +596,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(smem + L::kV + sv * L::kTile + a * kAtomBytes, &tm_v, &bar[QB_VFULL + sv],
                       a * 64, jj * kBlk, kvh, pol_kv);
         vissued = jj + 1;
+        if (jj == 0) {
+          // O_i goes to K stage 2, idle until K_2: the compute warps read it
+          // (for D) before that stage is loaded.
+          mbar_expect_tx(&bar[QB_O], L::kTile);
+          for (int a = 0; a < kAtoms; ++a)
+            tma_load_3d(smem + L::kK + 2 * L::kTile + a * kAtomBytes, &tm_o, &bar[QB_O], a * 64,
+                        i * kBlk, bhq, pol_q);
+          o_issued = true;
+          // Read only now, off the path to the first MMA (see the dK/dV kernel).
+          if (*reinterpret_cast<volatile int*>(err) != kDevErrNone) *abort_flag = 1;
+        }
       }
       if (*abort_flag) {
         drain_wait(&bar[QB_Q], 0);
+        if (o_issued) drain_wait(&bar[QB_O], 0);
         for (int jj = (kissued > kDqKStages ? kissued - kDqKStages : 0); jj < kissued; ++jj)
           drain_wait(&bar[QB_KFULL + jj % kDqKStages], (jj / kDqKStages) & 1);
         for (int jj = (vissued > 2 ? vissued - 2 : 0); jj < vissued; ++jj)
           drain_wait(&bar[QB_VFULL + (jj & 1)], (jj >> 1) & 1);
       }
     }
-  } else if (run && warp == 5) {
+  } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_f16(kBlk, kBlk, BF16, false, false);  // S, dP
@@ -666,7 +683,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(&bar[QB_FINAL]);
       drain_wait(&bar[QB_FINAL], 0);
     }
-  } else if (run && warp < 4) {
+  } else if (warp < 4) {
     // ------------------------------------------------------------ compute: P, dS
     const int t = threadIdx.x;  // query row within the tile
     const int q = i * kBlk + t;
@@ -678,10 +695,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     const size_t g = static_cast<size_t>(bhq) * N + q;
     // Padding rows (q >= N) get LSE = +inf: P and dS are exactly 0 there.
     const float lse2 = (q < N) ? lse[g] * kLog2e : INFINITY;
-    const float dq_d = (q < N) ? Drow[g] : 0.f;
-    const uint64_t negd2 = f2_pack(-dq_d, -dq_d);
+    // D_q = sum_c dO_qc O_qc from the O_i and dO_i tiles the producer staged,
+    // computed once the first P is done (while the first dP MMA runs) and
+    // written out for the dK/dV kernel, which runs after this one.
+    auto row_d = [&]() -> float {
+      float dq_d = 0.f;
+      if (q < N) {
+        const uint8_t* dorow = smem + L::kdO + t * 128;
+        const uint8_t* orow = smem + L::kK + 2 * L::kTile + t * 128;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) {  // 16-byte chunk c of the row (128-byte swizzle)
+          const int off = (c / 8) * kAtomBytes + (((c % 8) ^ (t & 7)) * 16);
+          const uint4 w = *reinterpret_cast<const uint4*>(dorow + off);
+          const uint4 ov = *reinterpret_cast<const uint4*>(orow + off);
+          const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w};
+          const uint32_t dw[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 x = unpack2<BF16>(ow[e]);
+            const float2 y = unpack2<BF16>(dw[e]);
+            acc[e] = fmaf(x.x, y.x, acc[e]);
+            acc[e] = fmaf(x.y, y.y, acc[e]);
+          }
+        }
+        dq_d = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+        Drow[g] = dq_d;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar[QB_OFREE]);  // generic reads of K stage 2 done
+      return dq_d;
+    };
+    uint64_t negd2 = 0;
     bool ok = true;
-    for (int jj = 0; jj < n_j; ++jj) {
+    for (int jj = 0; ok && jj < n_j; ++jj) {
       ok = __all_sync(0xffffffffu, mbar_wait(&bar[QB_SFULL], jj & 1, abort_flag, err));
       if (!ok) break;
       tc_fence_after();
@@ -710,6 +757,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < kBlk; ++c)
           if (c > t) p[c] = 0.f;
+      }
+      if (jj == 0) {
+        // dO_i (with Q_i) and O_i have landed.
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar[QB_Q], 0, abort_flag, err) &&
+                                         mbar_wait(&bar[QB_O], 0, abort_flag, err));
+        if (!ok) break;
+        const float dd = row_d();
+        negd2 = f2_pack(-dd, -dd);
       }
       ok = __all_sync(0xffffffffu, mbar_wait(&bar[QB_DPFULL], jj & 1, abort_flag, err));
       // dS(j) overwrites the columns dQ(j-1) reads.
@@ -752,9 +807,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bar[QB_FINAL], 0, abort_flag, err));
     if (ok) {
+      // Q's last reader, S(n_j - 1), has completed: dQ is staged in its place.
       tc_fence_after();
-      store_rows_from_tmem<D, BF16>(tmem + lane_off + kColDQ,
-                                    reinterpret_cast<uint16_t*>(dq_out) + g * D, scale, q < N);
+      uint8_t* st_dq = smem + L::kQ;
+      stage_row_from_tmem<D, BF16>(tmem + lane_off + kColDQ, st_dq, t, scale);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0 && i * kBlk + 32 * warp < N) {
+#pragma unroll
+        for (int a = 0; a < kAtoms; ++a)
+          tma_store_3d(&tm_dq, st_dq + a * kAtomBytes + warp * 4096, a * 64, i * kBlk + 32 * warp, bhq);
+        bulk_commit_group();
+        bulk_wait_read_all();
+      }
     }
   }
 
@@ -775,25 +840,13 @@ int l2_head_group(long per_head_bytes) {
   return static_cast<int>(g < 1 ? 1 : (g > 64 ? 64 : g));
 }
 
-int grid_for(long work_items, int per_block) {
-  long blocks = (work_items + per_block - 1) / per_block;
-  const long cap = static_cast<long>(sm_count()) * 16;  // 16 resident 256-thread blocks per SM
-  if (blocks > cap) blocks = cap;
-  return static_cast<int>(blocks < 1 ? 1 : blocks);
-}
-
 template <int D, bool BF16>
 cudaError_t launch_bwd_t(const AttnShape& s, const BwdArgs& a, cudaStream_t stream) {
-  const long rows = static_cast<long>(s.B) * s.Hq * s.N;
-  fa_bwd_pre_kernel<D, BF16><<<grid_for(rows * (D / 8), 256), 256, 0, stream>>>(
-      static_cast<const uint4*>(a.o), static_cast<const uint4*>(a.dO), a.D, rows);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-
   const int T = (s.N + kBlk - 1) / kBlk;
   auto kdkdv = fa_bwd_dkdv_kernel<D, BF16>;
   constexpr int smem_kv = DkdvSmem<D>::kAlloc;
   const int slot = (D == 64 ? 0 : 2) + (BF16 ? 1 : 0);
+  cudaError_t e;
   if ((e = set_smem_once(reinterpret_cast<const void*>(kdkdv), smem_kv, 8 + slot)) != cudaSuccess)
     return e;
   auto kdq = fa_bwd_dq_kernel<D, BF16>;
@@ -801,17 +854,19 @@ cudaError_t launch_bwd_t(const AttnShape& s, const BwdArgs& a, cudaStream_t stre
   if ((e = set_smem_once(reinterpret_cast<const void*>(kdq), smem_q, 16 + slot)) != cudaSuccess)
     return e;
 
-  if (a.ev_before_dkdv && (e = cudaEventRecord(a.ev_before_dkdv, stream)) != cudaSuccess) return e;
-  kdkdv<<<dim3(static_cast<unsigned>(T * s.B * s.Hkv)), kThreads, smem_kv, stream>>>(
-      a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.lse, a.D, a.dk, a.dv, s.B * s.Hkv,
-      l2_head_group(4L * s.N * D * (s.Hq / s.Hkv)), s.Hq, s.Hkv, s.N, s.causal, s.scale, a.err);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // The dQ kernel runs first: besides dQ it writes D = rowsum(dO o O), which
+  // the dK/dV kernel reads.
   if (a.ev_before_dq && (e = cudaEventRecord(a.ev_before_dq, stream)) != cudaSuccess) return e;
   kdq<<<dim3(static_cast<unsigned>(T * s.B * s.Hq)), kThreads, smem_q, stream>>>(
-      a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.lse, a.D, a.dq, s.B * s.Hq, l2_head_group(4L * s.N * D),
-      s.Hq, s.Hkv, s.N, s.causal, s.scale, a.err);
+      a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dq, a.tm_o, a.lse, a.D,
+      s.B * s.Hq, l2_head_group(4L * s.N * D), s.Hq, s.Hkv, s.N, s.causal, s.scale, a.err);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if (a.ev_after_dq && (e = cudaEventRecord(a.ev_after_dq, stream)) != cudaSuccess) return e;
+  if (a.ev_before_dkdv && (e = cudaEventRecord(a.ev_before_dkdv, stream)) != cudaSuccess) return e;
+  kdkdv<<<dim3(static_cast<unsigned>(T * s.B * s.Hkv)), kThreads, smem_kv, stream>>>(
+      a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dk, a.tm_dv, a.lse, a.D, s.B * s.Hkv,
+      l2_head_group(4L * s.N * D * (s.Hq / s.Hkv)), s.Hq, s.Hkv, s.N, s.causal, s.scale, a.err);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (a.ev_after_dkdv && (e = cudaEventRecord(a.ev_after_dkdv, stream)) != cudaSuccess) return e;
   return cudaSuccess;
 }
 

@@ -25,20 +25,23 @@ struct FwdArgs {
 };
 
 struct BwdArgs {
-  CUtensorMap tm_q, tm_k, tm_v, tm_do;
+  CUtensorMap tm_q, tm_k, tm_v, tm_do, tm_o;
+  // Store maps over dq [B*Hq, N, d] and dk, dv [B*Hkv, N, d]: box {64, 32, 1},
+  // 128-byte swizzle (one warp's 32 rows of a 128-row tile per store).
+  CUtensorMap tm_dq, tm_dk, tm_dv;
   const void* o;
   const void* dO;
   const float* lse;
-  float* D;  // [B*Hq*N]
+  float* D;  // [B*Hq*N], written by the dQ kernel, read by the dK/dV kernel
   void* dq;
   void* dk;
   void* dv;
   int* err;
-  // may be null: recorded before the dK/dV kernel, between it and the dQ
-  // kernel, and after the dQ kernel
-  cudaEvent_t ev_before_dkdv;
+  // may be null: recorded before the dQ kernel, between it and the dK/dV
+  // kernel, and after the dK/dV kernel
   cudaEvent_t ev_before_dq;
-  cudaEvent_t ev_after_dq;
+  cudaEvent_t ev_before_dkdv;
+  cudaEvent_t ev_after_dkdv;
 };
 
 // Split-KV forward (decoding): q [B, Hq, Nq, d] seen as [B*Hkv, (Hq/Hkv)*Nq, d].

@@ -120,13 +120,14 @@ FA_API size_t fa_backward_workspace_size(int B, int Hq, int N, int d);
  * lse, and dO = dL/dO, writes dq, dk, dv (element type dtype).
  *
  * Steps, all on `stream`:
- *   1. D_i = rowsum(dO_i * O_i) into the workspace;
- *   2. per key/value tile, recompute S^T and P^T = exp(scale * K Q^T - LSE)
- *      block by block and accumulate dV += P^T dO and dK += scale * dS^T Q,
- *      with dS = P * (dO V^T - D), over all query tiles (and, for grouped
- *      query attention, over the KV head's query heads) inside one CTA;
- *   3. per query tile, recompute S and P the same way and accumulate
- *      dQ += scale * dS K over all key tiles inside one CTA.
+ *   1. per query tile, D_i = rowsum(dO_i * O_i) (written to the workspace),
+ *      then recompute S and P = exp(scale * Q K^T - LSE) block by block and
+ *      accumulate dQ += scale * dS K over all key tiles inside one CTA, with
+ *      dS = P * (dO V^T - D);
+ *   2. per key/value tile, recompute S^T and P^T the same way and accumulate
+ *      dV += P^T dO and dK += scale * dS^T Q over all query tiles (and, for
+ *      grouped query attention, over the KV head's query heads) inside one
+ *      CTA, reading D from the workspace.
  * The gradient is that of the definition: the primer's printed dS omits the
  * -D term and the scale factor, which this library applies (the oracle's
  * finite-difference checks fix the formula).  No atomic adds are used: every
@@ -180,16 +181,16 @@ FA_API int fa_backward_noalloc(const void* q, const void* k, const void* v, cons
                                int dtype, void* stream);
 
 /*
- * Profiling hook for the backward's two main kernels.  After this call, every
+ * Profiling hook for the backward's two kernels.  After this call, every
  * fa_backward issued from the calling host thread records, on its stream,
- * `before_dkdv` immediately before launching the dK/dV kernel, `before_dq`
- * between it and the dQ kernel, and `after_dq` immediately after the dQ
- * kernel; cudaEventElapsedTime between consecutive events is each kernel's
- * device time.  All are cudaEvent_t handles passed as void*, created and
+ * `before_dq` immediately before launching the dQ kernel (which runs first),
+ * `before_dkdv` between it and the dK/dV kernel, and `after_dkdv` immediately
+ * after the dK/dV kernel; cudaEventElapsedTime between consecutive events is
+ * each kernel's device time.  All are cudaEvent_t handles passed as void*, created and
  * owned by the caller; pass three NULLs to stop.  Thread-local; never
  * synchronises.  Returns FA_OK, or FA_ERR_INVALID if only some are NULL.
  */
-FA_API int fa_set_backward_event_hooks(void* before_dkdv, void* before_dq, void* after_dq);
+FA_API int fa_set_backward_event_hooks(void* before_dq, void* before_dkdv, void* after_dkdv);
 
 /*
  * Synchronises `stream`, then reads and clears the device error word that the
