@@ -46,10 +46,14 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
         lib.fa_forward.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp]
         lib.fa_forward.restype = i
+        lib.fa_forward_window.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp]
+        lib.fa_forward_window.restype = i
         lib.fa_backward_workspace_size.argtypes = [i, i, i, i]
         lib.fa_backward_workspace_size.restype = sz
         lib.fa_backward.argtypes = [vp] * 10 + [sz] + [i] * 6 + [f, i, vp]
         lib.fa_backward.restype = i
+        lib.fa_backward_window.argtypes = [vp] * 10 + [sz] + [i] * 6 + [f, i, vp]
+        lib.fa_backward_window.restype = i
         lib.fa_forward_splitkv_workspace_size.argtypes = [i] * 7
         lib.fa_forward_splitkv_workspace_size.restype = sz
         lib.fa_forward_splitkv.argtypes = [vp] * 5 + [i] * 6 + [f, i, i, vp, sz, vp]
@@ -108,11 +112,22 @@ def workspace_size(B: int, Hq: int, N: int, d: int) -> int:
     return int(load().fa_backward_workspace_size(B, Hq, N, d))
 
 
+def _window_arg(window, causal) -> int:
+    window = int(window)
+    if not causal:
+        raise ValueError("a sliding window is causal: pass causal=True with window")
+    if window < 1:
+        raise ValueError(f"window must be at least 1, got {window}")
+    return window
+
+
 def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
-            stream=None):
+            stream=None, window: int | None = None):
     """O = softmax(scale q k^T) v and the natural-log LSE per row, on the GPU.
 
     q: [B, Hq, N, d]; k, v: [B, Hkv, N, d]; fp16 or bf16, contiguous, CUDA.
+    window: with causal=True, a sliding window of that many keys (query i sees
+    keys i - window < k <= i), through fa_forward_window.
     Returns (o [B,Hq,N,d] in q's dtype, lse [B,Hq,N] float32).
     """
     B, Hq, N, d = q.shape
@@ -128,9 +143,14 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None,
         lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device)
     _check(out, "out", (B, Hq, N, d), q.dtype)
     _check(lse, "lse", (B, Hq, N), torch.float32)
-    rc = load().fa_forward(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                           lse.data_ptr(), B, Hq, Hkv, N, d, int(bool(causal)), float(scale),
-                           _dtype_code(q), _stream_handle(stream))
+    if window is not None:
+        rc = load().fa_forward_window(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                      lse.data_ptr(), B, Hq, Hkv, N, d, _window_arg(window, causal),
+                                      float(scale), _dtype_code(q), _stream_handle(stream))
+    else:
+        rc = load().fa_forward(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                               lse.data_ptr(), B, Hq, Hkv, N, d, int(bool(causal)), float(scale),
+                               _dtype_code(q), _stream_handle(stream))
     _raise(rc)
     return out, lse
 
@@ -167,8 +187,11 @@ def forward_splitkv(q, k, v, scale: float | None = None, num_splits: int = 0, ou
 
 
 def backward(q, k, v, o, lse, dO, causal: bool = False, scale: float | None = None, dq=None,
-             dk=None, dv=None, workspace=None, stream=None):
-    """dq, dk, dv of O = softmax(scale q k^T) v given the forward's o, lse and dO = dL/dO."""
+             dk=None, dv=None, workspace=None, stream=None, window: int | None = None):
+    """dq, dk, dv of O = softmax(scale q k^T) v given the forward's o, lse and dO = dL/dO.
+
+    window: the forward's sliding window (with causal=True), through fa_backward_window.
+    """
     B, Hq, N, d = q.shape
     Hkv = k.shape[1]
     for t, name, H in ((q, "q", Hq), (k, "k", Hkv), (v, "v", Hkv), (o, "o", Hq), (dO, "dO", Hq)):
@@ -187,11 +210,16 @@ def backward(q, k, v, o, lse, dO, causal: bool = False, scale: float | None = No
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
     if workspace.numel() * workspace.element_size() < ws_bytes:
         raise ValueError(f"workspace must hold at least {ws_bytes} bytes")
-    rc = load().fa_backward(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                            dO.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
-                            workspace.data_ptr(), workspace.numel() * workspace.element_size(),
-                            B, Hq, Hkv, N, d, int(bool(causal)), float(scale), _dtype_code(q),
-                            _stream_handle(stream))
+    lib = load()
+    ptrs = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dO.data_ptr(),
+            dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(),
+            workspace.numel() * workspace.element_size())
+    if window is not None:
+        rc = lib.fa_backward_window(*ptrs, B, Hq, Hkv, N, d, _window_arg(window, causal),
+                                    float(scale), _dtype_code(q), _stream_handle(stream))
+    else:
+        rc = lib.fa_backward(*ptrs, B, Hq, Hkv, N, d, int(bool(causal)), float(scale),
+                             _dtype_code(q), _stream_handle(stream))
     _raise(rc)
     return dq, dk, dv
 

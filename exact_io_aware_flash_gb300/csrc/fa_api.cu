@@ -192,9 +192,15 @@ const char* fa_version(void) { return "fa-gb300 0.1.0 (sm_103a, tcgen05/TMEM/TMA
 
 const char* fa_last_error(void) { return t_last_error.c_str(); }
 
-int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
-               int Hkv, int N, int d, int causal, float scale, int dtype, void* stream) {
-  t_last_error.clear();
+}  // extern "C"
+
+namespace {
+
+// Shared body of fa_forward and fa_forward_window (window > 0: causal sliding
+// window narrower than N; 0: none).
+int forward_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                 int Hkv, int N, int d, int causal, int window, float scale, int dtype,
+                 void* stream) {
   if (!q || !k || !v || !o || !lse) return fail(FA_ERR_INVALID, "null tensor pointer");
   int rc = check_common(B, Hq, Hkv, N, d, scale, dtype);
   if (rc) return rc;
@@ -202,7 +208,7 @@ int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse,
     return fail(FA_ERR_UNSUPPORTED, "all tensor pointers must be 16-byte aligned");
   DeviceState* st = nullptr;
   if ((rc = get_device_state(&st))) return rc;
-  fa::AttnShape s{B, Hq, Hkv, N, d, causal ? 1 : 0, scale, dtype == FA_DTYPE_BF16};
+  fa::AttnShape s{B, Hq, Hkv, N, d, causal ? 1 : 0, scale, dtype == FA_DTYPE_BF16, window};
   fa::FwdArgs a{};
   if ((rc = encode_tile_map(&a.tm_q, q, B * Hq, N, d, s.bf16, "q"))) return rc;
   if ((rc = encode_tile_map(&a.tm_k, k, B * Hkv, N, d, s.bf16, "k"))) return rc;
@@ -213,6 +219,26 @@ int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse,
   cudaError_t e = fa::launch_forward(s, a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(FA_ERR_CUDA, "forward launch: %s", cudaGetErrorString(e));
   return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+               int Hkv, int N, int d, int causal, float scale, int dtype, void* stream) {
+  t_last_error.clear();
+  return forward_impl(q, k, v, o, lse, B, Hq, Hkv, N, d, causal, 0, scale, dtype, stream);
+}
+
+int fa_forward_window(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                      int Hq, int Hkv, int N, int d, int window, float scale, int dtype,
+                      void* stream) {
+  t_last_error.clear();
+  if (window < 1) return fail(FA_ERR_INVALID, "window must be at least 1 (got %d)", window);
+  // A window of N or more keys hides nothing that causal masking does not.
+  return forward_impl(q, k, v, o, lse, B, Hq, Hkv, N, d, 1, window < N ? window : 0, scale, dtype,
+                      stream);
 }
 
 namespace {
@@ -309,11 +335,15 @@ size_t fa_backward_workspace_size(int B, int Hq, int N, int d) {
   return round_up(rows * 4, 256);
 }
 
-int fa_backward(const void* q, const void* k, const void* v, const void* o, const float* lse,
-                const void* dO, void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
-                int B, int Hq, int Hkv, int N, int d, int causal, float scale, int dtype,
-                void* stream) {
-  t_last_error.clear();
+}  // extern "C"
+
+namespace {
+
+// Shared body of fa_backward and fa_backward_window (window as in forward_impl).
+int backward_impl(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                  const void* dO, void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
+                  int B, int Hq, int Hkv, int N, int d, int causal, int window, float scale,
+                  int dtype, void* stream) {
   if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv || !workspace)
     return fail(FA_ERR_INVALID, "null tensor pointer");
   int rc = check_common(B, Hq, Hkv, N, d, scale, dtype);
@@ -328,7 +358,7 @@ int fa_backward(const void* q, const void* k, const void* v, const void* o, cons
     if (!aligned16(p)) return fail(FA_ERR_UNSUPPORTED, "all tensor pointers must be 16-byte aligned");
   DeviceState* st = nullptr;
   if ((rc = get_device_state(&st))) return rc;
-  fa::AttnShape s{B, Hq, Hkv, N, d, causal ? 1 : 0, scale, dtype == FA_DTYPE_BF16};
+  fa::AttnShape s{B, Hq, Hkv, N, d, causal ? 1 : 0, scale, dtype == FA_DTYPE_BF16, window};
   fa::BwdArgs a{};
   if ((rc = encode_tile_map(&a.tm_q, q, B * Hq, N, d, s.bf16, "q"))) return rc;
   if ((rc = encode_tile_map(&a.tm_k, k, B * Hkv, N, d, s.bf16, "k"))) return rc;
@@ -352,6 +382,29 @@ int fa_backward(const void* q, const void* k, const void* v, const void* o, cons
   cudaError_t e = fa::launch_backward(s, a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(FA_ERR_CUDA, "backward launch: %s", cudaGetErrorString(e));
   return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_backward(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                const void* dO, void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
+                int B, int Hq, int Hkv, int N, int d, int causal, float scale, int dtype,
+                void* stream) {
+  t_last_error.clear();
+  return backward_impl(q, k, v, o, lse, dO, dq, dk, dv, workspace, ws_bytes, B, Hq, Hkv, N, d,
+                       causal, 0, scale, dtype, stream);
+}
+
+int fa_backward_window(const void* q, const void* k, const void* v, const void* o,
+                       const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                       void* workspace, size_t ws_bytes, int B, int Hq, int Hkv, int N, int d,
+                       int window, float scale, int dtype, void* stream) {
+  t_last_error.clear();
+  if (window < 1) return fail(FA_ERR_INVALID, "window must be at least 1 (got %d)", window);
+  return backward_impl(q, k, v, o, lse, dO, dq, dk, dv, workspace, ws_bytes, B, Hq, Hkv, N, d, 1,
+                       window < N ? window : 0, scale, dtype, stream);
 }
 
 int fa_set_backward_event_hooks(void* before_dq, void* before_dkdv, void* after_dkdv) {

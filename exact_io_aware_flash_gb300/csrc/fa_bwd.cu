@@ -124,6 +124,13 @@ __device__ __forceinline__ void stage_row_from_tmem(uint32_t taddr, uint8_t* til
   }
 }
 
+// First key tile a causal sliding window of `window` keys exposes to query
+// tile t: its first row, t*128, sees keys t*128 - window + 1 .. t*128.
+__device__ __forceinline__ int window_first_tile(int t, int window) {
+  const int first_key = t * kBlk - window + 1;
+  return first_key > 0 ? first_key / kBlk : 0;
+}
+
 // ------------------------------------------------------------------ dK, dV
 template <int D>
 struct DkdvSmem {
@@ -153,13 +160,17 @@ enum DkdvBars {
   KB_N = 12
 };
 
-template <int D, bool BF16>
+// WIN: causal sliding window of `window` keys (key k visible to query q iff
+// q - window < k <= q): key tile j meets only the query tiles its keys are
+// visible to, and the window's edge is masked element-wise.
+template <int D, bool BF16, bool WIN>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                        const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
                        const float* __restrict__ lse, const float* __restrict__ Drow, int heads,
-                       int head_group, int Hq, int Hkv, int N, int causal, float scale, int* err) {
+                       int head_group, int Hq, int Hkv, int N, int causal, int window, float scale,
+                       int* err) {
   using L = DkdvSmem<D>;
   constexpr int kAtoms = D / 64;
   extern __shared__ uint8_t smem_raw[];
@@ -180,7 +191,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int hkv = bkv % Hkv;
   const int group = Hq / Hkv;
   const int i0 = causal ? j : 0;
-  const int n_i = T - i0;
+  // Last query tile that sees a key of tile j: keys up to j*128 + 127 are
+  // visible to queries up to j*128 + 126 + window.
+  int i_last = T - 1;
+  if (WIN) {
+    const int qmax = (j * kBlk + kBlk - 2 + window) / kBlk;
+    i_last = qmax < T - 1 ? qmax : T - 1;
+  }
+  const int n_i = i_last - i0 + 1;
   const int n_it = group * n_i;
   constexpr uint32_t kColDV = 0, kColDK = 128, kColS = 256, kColDP = 384;
 
@@ -386,6 +404,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < kBlk; ++c)
           if (c < t) p[c] = 0.f;
       }
+      if (WIN && (i - j) * kBlk + kBlk - 1 >= window) {
+        // The window's edge crosses this tile: query i*128 + c sees key
+        // j*128 + t iff i*128 + c - window < j*128 + t.
+        const int lim_c = (j - i) * kBlk + t + window;
+#pragma unroll
+        for (int c = 0; c < kBlk; ++c)
+          if (c >= lim_c) p[c] = 0.f;
+      }
 #pragma unroll
       for (int c = 0; c < kBlk; c += 32) {
         uint32_t pk[16];
@@ -514,14 +540,16 @@ enum DqBars {
   QB_N = 20
 };
 
-template <int D, bool BF16>
+// WIN: causal sliding window (see the dK/dV kernel): query tile i meets only
+// the key tiles its window reaches.
+template <int D, bool BF16, bool WIN>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                      const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_o,
                      const float* __restrict__ lse, float* __restrict__ Drow, int heads,
                      int head_group, int Hq, int Hkv, int N,
-                     int causal, float scale, int* err) {
+                     int causal, int window, float scale, int* err) {
   using L = DqSmem<D>;
   constexpr int kAtoms = D / 64;
   extern __shared__ uint8_t smem_raw[];
@@ -541,7 +569,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int b = bhq / Hq;
   const int hq = bhq % Hq;
   const int kvh = b * Hkv + hq / (Hq / Hkv);
-  const int n_j = causal ? i + 1 : T;
+  const int j_lo = WIN ? window_first_tile(i, window) : 0;  // first key tile visited
+  const int n_j = causal ? i + 1 - j_lo : T;
   constexpr uint32_t kColDQ = 0, kColS = 128, kColDP = 256, kColDS = 384;
 
   if (threadIdx.x == 0) {
@@ -588,13 +617,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_expect_tx(&bar[QB_KFULL + sk], L::kTile);
         for (int a = 0; a < kAtoms; ++a)
           tma_load_3d(smem + L::kK + sk * L::kTile + a * kAtomBytes, &tm_k, &bar[QB_KFULL + sk],
-                      a * 64, jj * kBlk, kvh, pol_kv);
+                      a * 64, (j_lo + jj) * kBlk, kvh, pol_kv);
         kissued = jj + 1;
         if (!mbar_wait(&bar[QB_VEMPTY + sv], pv ^ 1, abort_flag, err)) break;
         mbar_expect_tx(&bar[QB_VFULL + sv], L::kTile);
         for (int a = 0; a < kAtoms; ++a)
           tma_load_3d(smem + L::kV + sv * L::kTile + a * kAtomBytes, &tm_v, &bar[QB_VFULL + sv],
-                      a * 64, jj * kBlk, kvh, pol_kv);
+                      a * 64, (j_lo + jj) * kBlk, kvh, pol_kv);
         vissued = jj + 1;
         if (jj == 0) {
           // O_i goes to K stage 2, idle until K_2: the compute warps read it
@@ -753,10 +782,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           p[c + 1] = ex2_approx(a1);
         }
       }
-      if (causal && jj == i) {  // key j*128 + c after query i*128 + t is masked
+      const int kt = j_lo + jj;  // key tile
+      if (causal && kt == i) {  // key kt*128 + c after query i*128 + t is masked
 #pragma unroll
         for (int c = 0; c < kBlk; ++c)
           if (c > t) p[c] = 0.f;
+      }
+      if (WIN && kt * kBlk + window <= i * kBlk + kBlk - 1) {
+        // The window's edge crosses this tile: key kt*128 + c is visible to
+        // query i*128 + t iff it is greater than i*128 + t - window.
+        const int lim = (i - kt) * kBlk + t - window;
+#pragma unroll
+        for (int c = 0; c < kBlk; ++c)
+          if (c <= lim) p[c] = 0.f;
       }
       if (jj == 0) {
         // dO_i (with Q_i) and O_i have landed.
@@ -840,16 +878,16 @@ int l2_head_group(long per_head_bytes) {
   return static_cast<int>(g < 1 ? 1 : (g > 64 ? 64 : g));
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool WIN>
 cudaError_t launch_bwd_t(const AttnShape& s, const BwdArgs& a, cudaStream_t stream) {
   const int T = (s.N + kBlk - 1) / kBlk;
-  auto kdkdv = fa_bwd_dkdv_kernel<D, BF16>;
+  auto kdkdv = fa_bwd_dkdv_kernel<D, BF16, WIN>;
   constexpr int smem_kv = DkdvSmem<D>::kAlloc;
-  const int slot = (D == 64 ? 0 : 2) + (BF16 ? 1 : 0);
+  const int slot = (WIN ? 4 : 0) + (D == 64 ? 0 : 2) + (BF16 ? 1 : 0);
   cudaError_t e;
   if ((e = set_smem_once(reinterpret_cast<const void*>(kdkdv), smem_kv, 8 + slot)) != cudaSuccess)
     return e;
-  auto kdq = fa_bwd_dq_kernel<D, BF16>;
+  auto kdq = fa_bwd_dq_kernel<D, BF16, WIN>;
   constexpr int smem_q = DqSmem<D>::kAlloc;
   if ((e = set_smem_once(reinterpret_cast<const void*>(kdq), smem_q, 16 + slot)) != cudaSuccess)
     return e;
@@ -859,12 +897,13 @@ cudaError_t launch_bwd_t(const AttnShape& s, const BwdArgs& a, cudaStream_t stre
   if (a.ev_before_dq && (e = cudaEventRecord(a.ev_before_dq, stream)) != cudaSuccess) return e;
   kdq<<<dim3(static_cast<unsigned>(T * s.B * s.Hq)), kThreads, smem_q, stream>>>(
       a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dq, a.tm_o, a.lse, a.D,
-      s.B * s.Hq, l2_head_group(4L * s.N * D), s.Hq, s.Hkv, s.N, s.causal, s.scale, a.err);
+      s.B * s.Hq, l2_head_group(4L * s.N * D), s.Hq, s.Hkv, s.N, s.causal, s.window, s.scale, a.err);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (a.ev_before_dkdv && (e = cudaEventRecord(a.ev_before_dkdv, stream)) != cudaSuccess) return e;
   kdkdv<<<dim3(static_cast<unsigned>(T * s.B * s.Hkv)), kThreads, smem_kv, stream>>>(
       a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dk, a.tm_dv, a.lse, a.D, s.B * s.Hkv,
-      l2_head_group(4L * s.N * D * (s.Hq / s.Hkv)), s.Hq, s.Hkv, s.N, s.causal, s.scale, a.err);
+      l2_head_group(4L * s.N * D * (s.Hq / s.Hkv)), s.Hq, s.Hkv, s.N, s.causal, s.window, s.scale,
+      a.err);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (a.ev_after_dkdv && (e = cudaEventRecord(a.ev_after_dkdv, stream)) != cudaSuccess) return e;
   return cudaSuccess;
@@ -877,8 +916,14 @@ size_t backward_smem_bytes(int d) {
 }
 
 cudaError_t launch_backward(const AttnShape& s, const BwdArgs& a, cudaStream_t stream) {
-  if (s.d == 64) return s.bf16 ? launch_bwd_t<64, true>(s, a, stream) : launch_bwd_t<64, false>(s, a, stream);
-  return s.bf16 ? launch_bwd_t<128, true>(s, a, stream) : launch_bwd_t<128, false>(s, a, stream);
+  if (s.window > 0) {  // causal sliding window
+    if (s.d == 64)
+      return s.bf16 ? launch_bwd_t<64, true, true>(s, a, stream) : launch_bwd_t<64, false, true>(s, a, stream);
+    return s.bf16 ? launch_bwd_t<128, true, true>(s, a, stream) : launch_bwd_t<128, false, true>(s, a, stream);
+  }
+  if (s.d == 64)
+    return s.bf16 ? launch_bwd_t<64, true, false>(s, a, stream) : launch_bwd_t<64, false, false>(s, a, stream);
+  return s.bf16 ? launch_bwd_t<128, true, false>(s, a, stream) : launch_bwd_t<128, false, false>(s, a, stream);
 }
 
 }  // namespace fa

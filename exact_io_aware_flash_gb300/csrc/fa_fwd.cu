@@ -108,12 +108,22 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // One work item: a pair of 128-row query tiles (A = 2p, B = 2p + 1) of one head.
+// The item streams key tiles loA .. loA + nKV - 1; tile X visits nX of them,
+// starting at key tile loX.
 struct FwdItem {
-  int bh, kvh, tA, tB, nA, nB, nKV;
+  int bh, kvh, tA, tB, nA, nB, nKV, loA, loB;
 };
 
+// First key tile a causal sliding window of `window` keys exposes to query
+// tile t: its first row, t*128, sees keys t*128 - window + 1 .. t*128.
+__device__ __forceinline__ int window_first_tile(int t, int window) {
+  const int first_key = t * kBM - window + 1;
+  return first_key > 0 ? first_key / kBN : 0;
+}
+
+template <bool WIN>
 __device__ __forceinline__ FwdItem decode_item(int item, int heads, int head_group, int Hq,
-                                               int Hkv, int T, int causal) {
+                                               int Hkv, int T, int causal, int window) {
   const int pairs = (T + 1) / 2;
   // Groups of heads whose K and V stay in L2; heaviest causal pairs first.
   const WorkItem wi = grouped_heavy_first(item, heads, pairs, head_group);
@@ -126,9 +136,12 @@ __device__ __forceinline__ FwdItem decode_item(int item, int heads, int head_gro
   it.tA = 2 * pair;
   it.tB = 2 * pair + 1;
   const bool hasB = it.tB < T;
-  it.nA = causal ? it.tA + 1 : T;
-  it.nB = hasB ? (causal ? it.tB + 1 : T) : 0;
-  it.nKV = it.nA > it.nB ? it.nA : it.nB;
+  it.loA = WIN ? window_first_tile(it.tA, window) : 0;
+  it.loB = (WIN && hasB) ? window_first_tile(it.tB, window) : it.loA;
+  it.nA = causal ? it.tA + 1 - it.loA : T;
+  it.nB = hasB ? (causal ? it.tB + 1 - it.loB : T) : 0;
+  const int endB = it.loB - it.loA + it.nB;  // stream tiles tile B needs
+  it.nKV = it.nA > endB ? it.nA : endB;
   return it;
 }
 
@@ -136,12 +149,17 @@ __device__ __forceinline__ FwdItem decode_item(int item, int heads, int head_gro
 // takes over the items of CTAs that have not started yet (cluster launch
 // control), so one CTA runs many items back to back and the next item's Q
 // loads and first S MMA overlap the current item's last softmax and epilogue.
-template <int D, bool BF16>
+// WIN: causal sliding window of `window` keys (key k visible to query i iff
+// i - window < k <= i): each query tile visits only the key tiles its window
+// reaches, and the window's lower edge is masked element-wise ("Flash
+// Attention" (aiwiki.ai), sections "Features" and "Block-sparse
+// FlashAttention": blocks a mask leaves empty are skipped).
+template <int D, bool BF16, bool WIN>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, void* __restrict__ out,
                   float* __restrict__ lse_out, int heads, int head_group, int Hq, int Hkv, int N,
-                  int causal, float scale_log2, int* err) {
+                  int causal, int window, float scale_log2, int* err) {
   using L = FwdSmem<D>;
   constexpr int kAtoms = D / 64;
   extern __shared__ uint8_t smem_raw[];
@@ -213,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         item_slot[slot] = item;
         mbar_arrive(&bar[BITEMFULL + slot]);  // release: the slot write is visible to waiters
         if (item < 0) break;
-        const FwdItem it = decode_item(item, heads, head_group, Hq, Hkv, T, causal);
+        const FwdItem it = decode_item<WIN>(item, heads, head_group, Hq, Hkv, T, causal, window);
         // Query tiles: buffer X is free once the previous item's last S_X has completed.
         for (int X = 0; X < 2 && ok; ++X) {
           const int nX = X ? it.nB : it.nA;
@@ -234,13 +252,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_expect_tx(&bar[BKFULL + sk], L::kTile);
           for (int a = 0; a < kAtoms; ++a)
             tma_load_3d(smem + L::kK + sk * L::kTile + a * kAtomBytes, &tm_k, &bar[BKFULL + sk],
-                        a * 64, j * kBN, it.kvh, pol_kv);
+                        a * 64, (it.loA + j) * kBN, it.kvh, pol_kv);
           kdone = kv + 1;
           if (!(ok = mbar_wait(&bar[BVEMPTY + sv], ((kv / kVStages) & 1) ^ 1, abort_flag, err))) break;
           mbar_expect_tx(&bar[BVFULL + sv], L::kTile);
           for (int a = 0; a < kAtoms; ++a)
             tma_load_3d(smem + L::kV + sv * L::kTile + a * kAtomBytes, &tm_v, &bar[BVFULL + sv],
-                        a * 64, j * kBN, it.kvh, pol_kv);
+                        a * 64, (it.loA + j) * kBN, it.kvh, pol_kv);
           vdone = kv + 1;
         }
         if (!ok) break;
@@ -324,12 +342,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&bar[BITEMEMPTY + (count & 1)]);
       if (item < 0) break;
       if (lane == 0) {
-        const FwdItem it = decode_item(item, heads, head_group, Hq, Hkv, T, causal);
+        const FwdItem it = decode_item<WIN>(item, heads, head_group, Hq, Hkv, T, causal, window);
         const int nX = X ? it.nB : it.nA;
-        if (nX > 0) {
-          const int stk0 = kv % kKStages;
+        // Key tiles of the item's stream this query tile does not visit (under
+        // a sliding window, tile B skips the first one; under causal masking
+        // tile A skips the last) still need this issuer's release.  It consumes
+        // them like the others -- waits until the tile has landed, then
+        // releases it -- so that its view of each ring stays in step: every
+        // wait on a full barrier is then for the phase right after the last
+        // one it observed, which a parity wait can tell apart.
+        auto skip_tile = [&](int u) -> bool {
+          const int stk = u % kKStages;
+          const int stv = u % kVStages;
+          if (!mbar_wait(&bar[BKFULL + stk], (u / kKStages) & 1, abort_flag, err)) return false;
+          if (!mbar_wait(&bar[BVFULL + stv], (u / kVStages) & 1, abort_flag, err)) return false;
+          mbar_arrive(&bar[BKEMPTY + stk]);
+          mbar_arrive(&bar[BVEMPTY + stv]);
+          return true;
+        };
+        const int lead = (WIN && X) ? it.loB - it.loA : 0;
+        for (int j = 0; ok && j < lead; ++j) ok = skip_tile(kv + j);
+        const int base = kv + lead;  // ring position of this tile's first key tile
+        if (ok && nX > 0) {
+          const int stk0 = base % kKStages;
           ok = mbar_wait(&bar[BQFULL + X], quse & 1, abort_flag, err) &&
-               mbar_wait(&bar[BKFULL + stk0], (kv / kKStages) & 1, abort_flag, err);
+               mbar_wait(&bar[BKFULL + stk0], (base / kKStages) & 1, abort_flag, err);
           // The previous item's last PV reads P from the S columns.
           if (ok && xs > 0) ok = mbar_wait(&bar[BODONE + X], (xs - 1) & 1, abort_flag, err);
           if (ok) {
@@ -338,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (nX == 1) mma_commit(&bar[BQEMPTY + X]);
           }
           for (int j = 0; ok && j < nX; ++j) {
-            const int u = kv + j;
+            const int u = base + j;
             const int stv = u % kVStages;
             if (!(ok = mbar_wait(&bar[BVFULL + stv], (u / kVStages) & 1, abort_flag, err))) break;
             if (!(ok = mbar_wait(&bar[BPFULL + X], (xs + j) & 1, abort_flag, err))) break;
@@ -356,20 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           xs += nX;
           ++quse;
         }
-        // Key tiles this query tile does not visit still need this issuer's
-        // release.  It consumes them like the others -- waits until the tile
-        // has landed, then releases it -- so that its view of each ring stays
-        // in step: every wait on a full barrier is then for the phase right
-        // after the last one it observed, which a parity wait can tell apart.
-        for (int j = nX; ok && j < it.nKV; ++j) {
-          const int u = kv + j;
-          const int stk = u % kKStages;
-          const int stv = u % kVStages;
-          if (!(ok = mbar_wait(&bar[BKFULL + stk], (u / kKStages) & 1, abort_flag, err))) break;
-          if (!(ok = mbar_wait(&bar[BVFULL + stv], (u / kVStages) & 1, abort_flag, err))) break;
-          mbar_arrive(&bar[BKEMPTY + stk]);
-          mbar_arrive(&bar[BVEMPTY + stv]);
-        }
+        for (int j = lead + nX; ok && j < it.nKV; ++j) ok = skip_tile(kv + j);
         kv += it.nKV;
       }
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -405,9 +429,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar[BITEMEMPTY + (count & 1)]);
       if (item < 0) break;
-      const FwdItem it = decode_item(item, heads, head_group, Hq, Hkv, T, causal);
+      const FwdItem it = decode_item<WIN>(item, heads, head_group, Hq, Hkv, T, causal, window);
       const int t = X ? it.tB : it.tA;
       const int nX = X ? it.nB : it.nA;
+      const int loX = X ? it.loB : it.loA;  // key tile of round 0
       const int m = it.nA < it.nB ? it.nA : it.nB;  // rounds both tiles have
       const int q = t * kBM + r;
       float m_run = -INFINITY;
@@ -445,8 +470,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < kBN; c += 32) tmem_ld32(tS + c, x + c);
         tmem_ld_wait();
         reg_fence<kBN>(x);
-        const int kbase = j * kBN;
-        const bool diag = causal && (j == t);
+        const int kbase = (loX + j) * kBN;
+        const bool diag = causal && (loX + j == t);
         // Scores stay raw when scale > 0 (the exponent is then one FFMA,
         // s * scale*log2(e) - m, and the row maximum of raw scores times the
         // positive factor is the maximum of the scaled scores); for scale <= 0
@@ -461,6 +486,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < kBN; ++c)
             if (c >= lim) x[c] = __float_as_uint(-INFINITY);
+        }
+        if (WIN && kbase + window <= t * kBM + kBM - 1) {
+          // The window's lower edge crosses this tile: key kbase + c is visible
+          // to query q iff kbase + c > q - window.  A row can be left with no
+          // visible key here (only in its first round); see m_use below.
+          const int lo_c = q - window + 1 - kbase;
+#pragma unroll
+          for (int c = 0; c < kBN; ++c)
+            if (c < lo_c) x[c] = __float_as_uint(-INFINITY);
         }
         // row maximum: eight independent chains (chain u: scores u, u+8, ...,
         // u+120) of three-input maxima, then a tree
@@ -489,9 +523,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             m_run = mx;
           }
         }
-        // exponent arguments and row sums two at a time (packed fp32)
+        // exponent arguments and row sums two at a time (packed fp32).  A row
+        // whose keys so far are all masked has m_run = -inf; its exponents are
+        // taken against 0 (all p = 0), and its next round rescales by 0.
+        const float m_use = (WIN && m_run == -INFINITY) ? 0.f : m_run;
         const uint64_t sfac2 = f2_pack(sfac, sfac);
-        const uint64_t negm2 = f2_pack(-m_run, -m_run);
+        const uint64_t negm2 = f2_pack(-m_use, -m_use);
         uint64_t rs2[2] = {0ull, 0ull};
 #pragma unroll
         for (int c = 0; c < kBN; c += 32) {
@@ -579,12 +616,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool WIN>
 cudaError_t launch_fwd_t(const AttnShape& s, const FwdArgs& a, cudaStream_t stream) {
-  auto kern = fa_fwd_kernel<D, BF16>;
+  auto kern = fa_fwd_kernel<D, BF16, WIN>;
   constexpr int smem = FwdSmem<D>::kAlloc;
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), smem,
-                                (D == 64 ? 0 : 2) + (BF16 ? 1 : 0));
+                                (WIN ? 4 : 0) + (D == 64 ? 0 : 2) + (BF16 ? 1 : 0));
   if (e != cudaSuccess) return e;
   const int T = (s.N + kBM - 1) / kBM;
   const int pairs = (T + 1) / 2;
@@ -597,7 +634,7 @@ cudaError_t launch_fwd_t(const AttnShape& s, const FwdArgs& a, cudaStream_t stre
   hg = hg < 1 ? 1 : (hg > 64 ? 64 : hg);
   kern<<<grid, kThreads, smem, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.o, a.lse, s.B * s.Hq,
                                          static_cast<int>(hg), s.Hq, s.Hkv, s.N, s.causal,
-                                         scale_log2, a.err);
+                                         s.window, scale_log2, a.err);
   return cudaGetLastError();
 }
 
@@ -608,8 +645,14 @@ size_t forward_smem_bytes(int d) {
 }
 
 cudaError_t launch_forward(const AttnShape& s, const FwdArgs& a, cudaStream_t stream) {
-  if (s.d == 64) return s.bf16 ? launch_fwd_t<64, true>(s, a, stream) : launch_fwd_t<64, false>(s, a, stream);
-  return s.bf16 ? launch_fwd_t<128, true>(s, a, stream) : launch_fwd_t<128, false>(s, a, stream);
+  if (s.window > 0) {  // causal sliding window
+    if (s.d == 64)
+      return s.bf16 ? launch_fwd_t<64, true, true>(s, a, stream) : launch_fwd_t<64, false, true>(s, a, stream);
+    return s.bf16 ? launch_fwd_t<128, true, true>(s, a, stream) : launch_fwd_t<128, false, true>(s, a, stream);
+  }
+  if (s.d == 64)
+    return s.bf16 ? launch_fwd_t<64, true, false>(s, a, stream) : launch_fwd_t<64, false, false>(s, a, stream);
+  return s.bf16 ? launch_fwd_t<128, true, false>(s, a, stream) : launch_fwd_t<128, false, false>(s, a, stream);
 }
 
 }  // namespace fa

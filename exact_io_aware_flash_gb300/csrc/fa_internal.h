@@ -14,6 +14,9 @@ struct AttnShape {
   int causal;
   float scale;
   int bf16;  // 1 = bfloat16, 0 = float16
+  // > 0: causal sliding window, key k visible to query i iff i - window < k <= i
+  // (requires causal = 1 and window < N); 0: none
+  int window;
 };
 
 // Tensor maps over [B*H, N, d] 16-bit tensors, box {64, 128, 1}, 128-byte swizzle.

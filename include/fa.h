@@ -84,6 +84,23 @@ FA_API int fa_forward(const void* q, const void* k, const void* v, void* o, floa
                int Hkv, int N, int d, int causal, float scale, int dtype, void* stream);
 
 /*
+ * Sliding-window (local) causal forward: like fa_forward with causal = 1, but
+ * query i attends only to the `window` most recent keys, i - window < k <= i
+ * ("Flash Attention" (aiwiki.ai), section "Features": local sliding windows;
+ * section "Block-sparse FlashAttention": blocks the mask leaves empty are
+ * skipped, so the work grows with the retained blocks, about N * window,
+ * instead of N^2 / 2).
+ *
+ * window >= 1 (FA_ERR_INVALID otherwise); window >= N gives exactly the causal
+ * result.  Key tiles outside every row's window are neither loaded nor
+ * computed; tiles the window's edge crosses are masked element-wise.  Outputs,
+ * layouts, errors, determinism and asynchrony as fa_forward.
+ */
+FA_API int fa_forward_window(const void* q, const void* k, const void* v, void* o, float* lse,
+                             int B, int Hq, int Hkv, int N, int d, int window, float scale,
+                             int dtype, void* stream);
+
+/*
  * Split-KV forward for decoding: a few query rows against a long key sequence
  * ("Flash Attention" (aiwiki.ai), section "Flash-Decoding": split the keys
  * into chunks, attend to each chunk with its own log-sum-exp, combine).
@@ -141,6 +158,18 @@ FA_API int fa_backward(const void* q, const void* k, const void* v, const void* 
                 const void* dO, void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
                 int B, int Hq, int Hkv, int N, int d, int causal, float scale, int dtype,
                 void* stream);
+
+/*
+ * Backward pass of fa_forward_window: the gradients of the sliding-window
+ * causal attention (i - window < k <= i) from the saved O and LSE.  Same
+ * arguments, workspace, outputs, errors and asynchrony as fa_backward, with
+ * `window` (>= 1) in place of `causal`; window >= N equals the causal
+ * backward.  Only the key/query tile pairs some window reaches are computed.
+ */
+FA_API int fa_backward_window(const void* q, const void* k, const void* v, const void* o,
+                              const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                              void* workspace, size_t ws_bytes, int B, int Hq, int Hkv, int N,
+                              int d, int window, float scale, int dtype, void* stream);
 
 /*
  * Backward pass that allocates nothing.  (Library-side addition: the attention

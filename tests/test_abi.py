@@ -98,3 +98,20 @@ def test_invalid_arguments_fail_before_device_work(lib):
     assert lib.fa_backward(fake, fake, fake, fake, fake, fake, fake, fake, fake, fake, 16,
                            1, 1, 1, 8, 64, 0, 1.0, 0, null) == 1
     assert b"workspace" in lib.fa_last_error()
+
+
+def test_window_entry_points_validate_before_device_work(lib):
+    fake = ctypes.c_void_p(4096)
+    null = ctypes.c_void_p(0)
+    # window must be at least 1
+    assert lib.fa_forward_window(fake, fake, fake, fake, fake, 1, 1, 1, 8, 64, 0, 1.0, 0, null) == 1
+    assert b"window" in lib.fa_last_error()
+    assert lib.fa_forward_window(fake, fake, fake, fake, fake, 1, 1, 1, 8, 64, -3, 1.0, 0, null) == 1
+    # the checks shared with fa_forward still apply
+    assert lib.fa_forward_window(null, fake, fake, fake, fake, 1, 1, 1, 8, 64, 4, 1.0, 0, null) == 1
+    assert lib.fa_forward_window(fake, fake, fake, fake, fake, 1, 1, 1, 8, 96, 4, 1.0, 0, null) == 2
+    assert lib.fa_backward_window(fake, fake, fake, fake, fake, fake, fake, fake, fake, fake, 1 << 20,
+                                  1, 1, 1, 8, 64, 0, 1.0, 0, null) == 1
+    assert lib.fa_backward_window(fake, fake, fake, fake, fake, fake, fake, fake, fake, fake, 16,
+                                  1, 1, 1, 8, 64, 4, 1.0, 0, null) == 1
+    assert b"workspace" in lib.fa_last_error()
