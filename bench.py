@@ -520,8 +520,8 @@ def workload_table(dev, peaks):
 
     from exact_io_aware_flash_gb300 import backward, forward, forward_splitkv, workspace_size
     from exact_io_aware_flash_gb300.flops import backward_flops, forward_bytes, forward_flops
-    from exact_io_aware_flash_gb300.synth import (BACKWARD_SWEEP_N, WORKLOADS, backward_sweep_shape,
-                                                  make_inputs)
+    from exact_io_aware_flash_gb300.synth import (BACKWARD_SWEEP_N, WORKLOADS, Shape,
+                                                  backward_sweep_shape, make_inputs)
 
     burst = peaks["bf16_tflops"]
     hbm = peaks["hbm_gbs"]
@@ -579,6 +579,26 @@ def workload_table(dev, peaks):
         bwd[f"N{N}"] = e
         del q, k, v, dO, o, lse, ws, dq, dk, dv
     out["backward_sweep"] = bwd
+    # sliding-window (local) causal attention, GQA 32/8, window 4096 over N = 16384
+    from exact_io_aware_flash_gb300.flops import backward_flops_window, forward_flops_window
+    B, Hq, Hkv, N, d, W = 1, 32, 8, 16384, 128, 4096
+    inp = make_inputs(Shape(B, Hq, Hkv, N, d), "bf16", seed=4096 + N)
+    q, k, v, dO = (inp[n].to(dev) for n in ("q", "k", "v", "dO"))
+    o, lse = forward(q, k, v, causal=True, window=W)
+    ws = torch.empty(workspace_size(B, Hq, N, d), dtype=torch.uint8, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ms_f = _graph_time(lambda: forward(q, k, v, causal=True, window=W, out=o, lse=lse), iters=10)
+    ms_b = _graph_time(lambda: backward(q, k, v, o, lse, dO, causal=True, window=W, dq=dq, dk=dk,
+                                        dv=dv, workspace=ws), iters=10)
+    ff, fb = forward_flops_window(B, Hq, N, d, W), backward_flops_window(B, Hq, N, d, W)
+    out["sliding_window"] = {
+        "shape": f"B{B} Hq{Hq} Hkv{Hkv} N{N} d{d} bf16, window {W} (key k visible to query i "
+                 f"iff i - {W} < k <= i)",
+        "flops": "4*d per visible (query, key) pair forward, 2.5x that backward",
+        "forward": {"ms": ms_f, "tflops": ff / ms_f / 1e9, "pct_of_bf16_burst": ff / ms_f / 1e9 / burst},
+        "backward": {"ms": ms_b, "tflops": fb / ms_b / 1e9, "pct_of_bf16_burst": fb / ms_b / 1e9 / burst},
+    }
+    del q, k, v, dO, o, lse, ws, dq, dk, dv
     # decoding (split-KV): one new query row per head against a 32k-token cache, GQA 32/8
     B, Hq, Hkv, Nk, d = 8, 32, 8, 32768, 128
     g = torch.Generator(device="cpu").manual_seed(4096)

@@ -25,6 +25,24 @@ def backward_flops(B: int, H: int, N: int, d: int, causal: bool) -> float:
     return 2.5 * forward_flops(B, H, N, d, causal)
 
 
+def window_pairs(N: int, window: int) -> int:
+    """Visible (query, key) pairs of a causal sliding window of ``window`` keys
+    over N positions (query i sees keys i - window < k <= i): sum_i min(i + 1, window)."""
+    w = min(window, N)
+    return w * (w + 1) // 2 + (N - w) * w
+
+
+def forward_flops_window(B: int, H: int, N: int, d: int, window: int) -> float:
+    """Two products of 2*d FLOPs per visible pair (the work a block-sparse
+    schedule that skips empty blocks needs, "Flash Attention" (aiwiki.ai),
+    section "Block-sparse FlashAttention")."""
+    return 4.0 * d * B * H * window_pairs(N, window)
+
+
+def backward_flops_window(B: int, H: int, N: int, d: int, window: int) -> float:
+    return 2.5 * forward_flops_window(B, H, N, d, window)
+
+
 def forward_bytes(B: int, Hq: int, Hkv: int, N: int, d: int, elt: int = 2) -> int:
     """Q, K, V read + O written (16-bit) + LSE written (fp32)."""
     return elt * N * d * B * (2 * Hq + 2 * Hkv) + 4 * B * Hq * N
