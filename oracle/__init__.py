@@ -15,6 +15,14 @@ Contents
     written in numpy fp64, used to check that the recurrence reproduces the
     definition.
 
+  * FP8 (e4m3) inputs (``e4m3_encode`` / ``e4m3_decode``, ``fp8_quantize_qk``,
+    ``fp8_quantize_v``, ``fp8_dequantize``, ``forward_fp8``): the definition of the
+    FlashAttention-3 low-precision forward's quantized inputs -- random-sign
+    Hadamard rotation of Q and K, one scale per 128-row block (Q, K) or per
+    channel (V), e4m3 codes -- and the plain attention over their values.
+  * ``fp8_baseline``: per-tensor FP8 attention, the baseline of the pages' FP8
+    error comparison.
+
 Citations are to the web pages the method is described on:
   "FlashAttention Primer: IO-Aware Attention, from FA1 to FA4" (oripoin.me),
   "Flash Attention" (aiwiki.ai), "FlashAttention" concept page (praveentn.live).
@@ -54,6 +62,20 @@ def _as_f64(x) -> np.ndarray:
     return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
 
 
+def _as_f32(x) -> np.ndarray:
+    if hasattr(x, "detach"):  # torch tensor: exact widening of the 16-bit values
+        x = x.detach().to("cpu").float().numpy()
+    return np.asarray(x, dtype=np.float32)
+
+
+def _fptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_float))
+
+
+def _u8ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8))
+
+
 def _ptr(a: np.ndarray):
     return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
 
@@ -79,6 +101,18 @@ class Oracle:
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = i
         self.lib = lib
+
+        u8p = ctypes.POINTER(ctypes.c_uint8)
+        fp = ctypes.POINTER(ctypes.c_float)
+        i8p = ctypes.POINTER(ctypes.c_int8)
+        lib.oracle_e4m3_encode_array.argtypes = [fp, u8p, ctypes.c_long]
+        lib.oracle_e4m3_encode_array.restype = i
+        lib.oracle_e4m3_decode_array.argtypes = [u8p, dp, ctypes.c_long]
+        lib.oracle_e4m3_decode_array.restype = i
+        lib.oracle_fp8_quantize_qk.argtypes = [fp, i8p, i, i, i, u8p, fp]
+        lib.oracle_fp8_quantize_qk.restype = i
+        lib.oracle_fp8_quantize_v.argtypes = [fp, i, i, i, u8p, fp]
+        lib.oracle_fp8_quantize_v.restype = i
 
     def num_threads(self) -> int:
         return int(self.lib.oracle_num_threads())
@@ -142,6 +176,64 @@ class Oracle:
             raise ValueError(f"oracle_backward_window failed with code {rc}")
         return dq, dk, dv
 
+    # ------------------------------------------------------------ FP8 (e4m3) inputs
+    def e4m3_encode(self, x) -> np.ndarray:
+        """Nearest e4m3 code of each fp32 value (ties to even, saturating at 448)."""
+        x = np.ascontiguousarray(_as_f32(x))
+        out = np.empty(x.shape, dtype=np.uint8)
+        rc = self.lib.oracle_e4m3_encode_array(_fptr(x), _u8ptr(out), x.size)
+        if rc:
+            raise ValueError(f"oracle_e4m3_encode_array failed with code {rc}")
+        return out
+
+    def e4m3_decode(self, codes) -> np.ndarray:
+        codes = np.ascontiguousarray(np.asarray(codes, dtype=np.uint8))
+        out = np.empty(codes.shape, dtype=np.float64)
+        rc = self.lib.oracle_e4m3_decode_array(_u8ptr(codes), _ptr(out), codes.size)
+        if rc:
+            raise ValueError(f"oracle_e4m3_decode_array failed with code {rc}")
+        return out
+
+    def fp8_quantize_qk(self, x, signs):
+        """Q or K [B, H, N, d] -> (codes uint8 [B, H, N, d], scales float32 [B, H, ceil(N/128)]).
+        signs: d values of +1/-1 (the random signs of the rotation), or None for no rotation."""
+        x = np.ascontiguousarray(_as_f32(x))
+        B, H, N, d = x.shape
+        codes = np.empty(x.shape, dtype=np.uint8)
+        scales = np.empty((B, H, (N + 127) // 128), dtype=np.float32)
+        sg = None if signs is None else np.ascontiguousarray(np.asarray(signs, dtype=np.int8))
+        rc = self.lib.oracle_fp8_quantize_qk(_fptr(x), None if sg is None else sg.ctypes.data_as(
+            ctypes.POINTER(ctypes.c_int8)), B * H, N, d, _u8ptr(codes), _fptr(scales))
+        if rc:
+            raise ValueError(f"oracle_fp8_quantize_qk failed with code {rc}")
+        return codes, scales
+
+    def fp8_quantize_v(self, v):
+        """V [B, H, N, d] -> (codes uint8 [B, H, N, d], scales float32 [B, H, d])."""
+        v = np.ascontiguousarray(_as_f32(v))
+        B, H, N, d = v.shape
+        codes = np.empty(v.shape, dtype=np.uint8)
+        scales = np.empty((B, H, d), dtype=np.float32)
+        rc = self.lib.oracle_fp8_quantize_v(_fptr(v), B * H, N, d, _u8ptr(codes), _fptr(scales))
+        if rc:
+            raise ValueError(f"oracle_fp8_quantize_v failed with code {rc}")
+        return codes, scales
+
+    def fp8_dequantize(self, q_codes, q_scales, k_codes, k_scales, v_codes, v_scales):
+        """fp64 values the codes stand for: code x scale of its block (Q, K) or channel (V)."""
+        def rows(codes, scales):
+            N = codes.shape[2]
+            per_row = np.repeat(np.asarray(scales, dtype=np.float64), 128, axis=2)[:, :, :N]
+            return self.e4m3_decode(codes) * per_row[..., None]
+        vh = self.e4m3_decode(v_codes) * np.asarray(v_scales, dtype=np.float64)[:, :, None, :]
+        return rows(q_codes, q_scales), rows(k_codes, k_scales), vh
+
+    def forward_fp8(self, q_codes, q_scales, k_codes, k_scales, v_codes, v_scales, causal: bool,
+                    scale: float):
+        """Attention (the plain definition, fp64) over the dequantized FP8 inputs."""
+        qh, kh, vh = self.fp8_dequantize(q_codes, q_scales, k_codes, k_scales, v_codes, v_scales)
+        return self.forward(qh, kh, vh, causal, scale)
+
     def backward(self, q, k, v, dO, causal: bool, scale: float):
         """dQ, dK, dV (and D = rowsum(dO * O)) of the definition, fp64.
 
@@ -198,3 +290,34 @@ def forward_window(q, k, v, window: int, scale: float):
 def backward_window(q, k, v, dO, window: int, scale: float):
     """See ``Oracle.backward_window``."""
     return _default().backward_window(q, k, v, dO, window, scale)
+
+
+def e4m3_encode(x):
+    """See ``Oracle.e4m3_encode``."""
+    return _default().e4m3_encode(x)
+
+
+def e4m3_decode(codes):
+    """See ``Oracle.e4m3_decode``."""
+    return _default().e4m3_decode(codes)
+
+
+def fp8_quantize_qk(x, signs):
+    """See ``Oracle.fp8_quantize_qk``."""
+    return _default().fp8_quantize_qk(x, signs)
+
+
+def fp8_quantize_v(v):
+    """See ``Oracle.fp8_quantize_v``."""
+    return _default().fp8_quantize_v(v)
+
+
+def fp8_dequantize(q_codes, q_scales, k_codes, k_scales, v_codes, v_scales):
+    """See ``Oracle.fp8_dequantize``."""
+    return _default().fp8_dequantize(q_codes, q_scales, k_codes, k_scales, v_codes, v_scales)
+
+
+def forward_fp8(q_codes, q_scales, k_codes, k_scales, v_codes, v_scales, causal: bool, scale: float):
+    """See ``Oracle.forward_fp8``."""
+    return _default().forward_fp8(q_codes, q_scales, k_codes, k_scales, v_codes, v_scales, causal,
+                                  scale)

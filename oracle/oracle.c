@@ -394,3 +394,150 @@ int oracle_backward(const double* q, const double* k, const double* v, const dou
     }
     return failed ? ORACLE_ENOMEM : ORACLE_OK;
 }
+
+/* ==================================================================== FP8 (e4m3) inputs
+ *
+ * The low-precision forward of FlashAttention-3 ("FlashAttention Primer", section
+ * "FlashAttention-3: Hopper asynchrony and FP8": block quantization and an incoherent
+ * rotation applied before quantization; "Flash Attention" (aiwiki.ai), section
+ * "FlashAttention-3": the transform is random signs followed by a Hadamard transform,
+ * applied to queries and keys alike, so their dot products are unchanged in real
+ * arithmetic while outliers are spread over all channels).  These functions define the
+ * quantized inputs; the attention over them is the plain definition above, applied to
+ * the dequantized values (code x scale).
+ *
+ * Readings where the pages leave a step open:
+ *   - Q and K: each row is multiplied by the signs s (+1/-1 per channel) and by the
+ *     Sylvester Hadamard matrix H_d (entries +-1) -- the unnormalised rotation, computed
+ *     in fp32 by the butterfly below -- then quantized with one scale per block of 128
+ *     rows of one head.  The dequantization scale carries 1/sqrt(d), which makes the
+ *     rotation orthogonal: (x s H / sqrt(d)) . (y s H / sqrt(d)) = x . y.
+ *   - V is not rotated (P V has no partner product to cancel a rotation) and gets one
+ *     scale per (head, channel), which factors out of P V exactly.
+ *   - Scales come from the block's largest magnitude: the largest element maps to 448,
+ *     the largest finite e4m3 value.
+ * Floating-point steps that decide a code are done in fp32 in a fixed order, so the
+ * codes are a definite function of the inputs (bit-exact comparisons are possible).
+ */
+
+/* e4m3: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits; no infinities;
+ * S.1111.111 is NaN, so the largest finite magnitude is 1.75 * 2^8 = 448.
+ * Exponent field e >= 1: (1 + m/8) * 2^(e-7); e = 0: (m/8) * 2^-6 (subnormal). */
+double oracle_e4m3_decode(int code) {
+    const int sign = (code >> 7) & 1;
+    const int e = (code >> 3) & 0xF;
+    const int m = code & 7;
+    if (e == 0xF && m == 7) return NAN;
+    const double mag = (e == 0) ? ldexp((double)m / 8.0, -6) : ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sign ? -mag : mag;
+}
+
+/* Nearest e4m3 value, ties to the even code (mantissa bit 0 clear), magnitudes beyond
+ * 448 saturate to 448; the sign of zero is kept.  Plain search over the 127 finite
+ * non-negative codes, which increase with the code. */
+int oracle_e4m3_encode(float x) {
+    if (isnan(x)) return 0x7F;
+    const int sign = signbit(x) ? 0x80 : 0;
+    const double a = fabs((double)x);
+    int lo = 0;
+    for (int c = 1; c <= 0x7E; ++c)
+        if (oracle_e4m3_decode(c) <= a) lo = c;
+    if (lo == 0x7E) return sign | 0x7E;
+    const double vlo = oracle_e4m3_decode(lo), vhi = oracle_e4m3_decode(lo + 1);
+    const double mid = 0.5 * (vlo + vhi);
+    int c;
+    if (a < mid) c = lo;
+    else if (a > mid) c = lo + 1;
+    else c = (lo & 1) ? lo + 1 : lo;
+    return sign | c;
+}
+
+/* x <- x H_d, unnormalised, in fp32, in place (d a power of two).  Stage h = 1, 2, 4,
+ * ..., d/2 replaces the pair (x[i], x[i+h]) for each i with bit h clear by
+ * (x[i] + x[i+h], x[i] - x[i+h]). */
+static void fwht_f32(float* x, int d) {
+    for (int h = 1; h < d; h <<= 1)
+        for (int i = 0; i < d; ++i)
+            if ((i & h) == 0) {
+                const float a = x[i], b = x[i + h];
+                x[i] = a + b;
+                x[i + h] = a - b;
+            }
+}
+
+/* Q or K: x [heads, N, d] (values of the 16-bit inputs, exactly widened to fp32).
+ * signs: d entries of +1/-1, or NULL for no rotation (per-block quantization only).
+ * Outputs codes [heads, N, d] and scales [heads, ceil(N/128)]:
+ *   y = x * s then y <- y H_d                     (if rotating)
+ *   amax = max |y| over the block's rows and channels
+ *   code = e4m3(y * (448 / amax))                 (fp32 division, then fp32 product)
+ *   scale = amax * c, c = fl32(1 / (448 sqrt(d))) rotating, fl32(1 / 448) not
+ * A block whose values are all zero gets scale 0 and codes e4m3(+-0). */
+int oracle_fp8_quantize_qk(const float* x, const signed char* signs, int heads, int N, int d,
+                           unsigned char* codes, float* scales) {
+    if (heads <= 0 || N <= 0 || d <= 0 || (d & (d - 1)) != 0 || !x || !codes || !scales)
+        return ORACLE_EINVAL;
+    const int T = (N + 127) / 128;
+    const float cfac = signs ? (float)(1.0 / (448.0 * sqrt((double)d))) : (float)(1.0 / 448.0);
+    float* y = (float*)malloc(sizeof(float) * (size_t)128 * d);
+    if (!y) return ORACLE_ENOMEM;
+    for (int h = 0; h < heads; ++h)
+        for (int t = 0; t < T; ++t) {
+            const int r0 = t * 128, r1 = (r0 + 128 < N) ? r0 + 128 : N;
+            float amax = 0.f;
+            for (int r = r0; r < r1; ++r) {
+                float* yr = y + (size_t)(r - r0) * d;
+                const float* xr = x + ((size_t)h * N + r) * d;
+                for (int c = 0; c < d; ++c) yr[c] = (signs && signs[c] < 0) ? -xr[c] : xr[c];
+                if (signs) fwht_f32(yr, d);
+                for (int c = 0; c < d; ++c)
+                    if (fabsf(yr[c]) > amax) amax = fabsf(yr[c]);
+            }
+            const float f = amax > 0.f ? 448.0f / amax : 0.f;
+            scales[(size_t)h * T + t] = amax * cfac;
+            for (int r = r0; r < r1; ++r)
+                for (int c = 0; c < d; ++c)
+                    codes[((size_t)h * N + r) * d + c] =
+                        (unsigned char)oracle_e4m3_encode(y[(size_t)(r - r0) * d + c] * f);
+        }
+    free(y);
+    return ORACLE_OK;
+}
+
+/* V: v [heads, N, d].  One scale per (head, channel):
+ *   amax_c = max over the head's N rows of |v_rc|
+ *   code = e4m3(v * (448 / amax_c)),  scale_c = amax_c * fl32(1/448)
+ * Outputs codes [heads, N, d] and scales [heads, d]. */
+int oracle_fp8_quantize_v(const float* v, int heads, int N, int d, unsigned char* codes,
+                          float* scales) {
+    if (heads <= 0 || N <= 0 || d <= 0 || !v || !codes || !scales) return ORACLE_EINVAL;
+    const float cfac = (float)(1.0 / 448.0);
+    for (int h = 0; h < heads; ++h)
+        for (int c = 0; c < d; ++c) {
+            float amax = 0.f;
+            for (int r = 0; r < N; ++r) {
+                const float a = fabsf(v[((size_t)h * N + r) * d + c]);
+                if (a > amax) amax = a;
+            }
+            const float f = amax > 0.f ? 448.0f / amax : 0.f;
+            scales[(size_t)h * d + c] = amax * cfac;
+            for (int r = 0; r < N; ++r) {
+                const size_t e = ((size_t)h * N + r) * d + c;
+                codes[e] = (unsigned char)oracle_e4m3_encode(v[e] * f);
+            }
+        }
+    return ORACLE_OK;
+}
+
+/* Element-wise front ends of the two functions above, for arrays. */
+int oracle_e4m3_encode_array(const float* x, unsigned char* out, long n) {
+    if (n < 0 || (n > 0 && (!x || !out))) return ORACLE_EINVAL;
+    for (long i = 0; i < n; ++i) out[i] = (unsigned char)oracle_e4m3_encode(x[i]);
+    return ORACLE_OK;
+}
+
+int oracle_e4m3_decode_array(const unsigned char* c, double* out, long n) {
+    if (n < 0 || (n > 0 && (!c || !out))) return ORACLE_EINVAL;
+    for (long i = 0; i < n; ++i) out[i] = oracle_e4m3_decode(c[i]);
+    return ORACLE_OK;
+}
