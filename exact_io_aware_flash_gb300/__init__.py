@@ -8,5 +8,6 @@ in hand-written tcgen05/TMEM/TMA kernels behind the C ABI of ``libfa.so``
     o, lse = forward(q, k, v, causal=True)
     dq, dk, dv = backward(q, k, v, o, lse, dO, causal=True)
 """
-from ._lib import (FAError, backward, check_errors, forward, forward_splitkv, load,  # noqa: F401
-                   selftest_bounded_wait, set_backward_event_hooks, version, workspace_size)
+from ._lib import (FAError, backward, check_errors, forward, forward_fp8, forward_splitkv,  # noqa: F401
+                   load, quantize_fp8, selftest_bounded_wait, set_backward_event_hooks, version,
+                   workspace_size)

@@ -54,6 +54,12 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.fa_backward.restype = i
         lib.fa_backward_window.argtypes = [vp] * 10 + [sz] + [i] * 6 + [f, i, vp]
         lib.fa_backward_window.restype = i
+        lib.fa_fp8_vt_stride.argtypes = [i]
+        lib.fa_fp8_vt_stride.restype = i
+        lib.fa_quantize_fp8.argtypes = [vp] * 10 + [i] * 6 + [vp]
+        lib.fa_quantize_fp8.restype = i
+        lib.fa_forward_fp8.argtypes = [vp] * 8 + [i] * 6 + [f, vp]
+        lib.fa_forward_fp8.restype = i
         lib.fa_forward_splitkv_workspace_size.argtypes = [i] * 7
         lib.fa_forward_splitkv_workspace_size.restype = sz
         lib.fa_forward_splitkv.argtypes = [vp] * 5 + [i] * 6 + [f, i, i, vp, sz, vp]
@@ -151,6 +157,71 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None,
         rc = load().fa_forward(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                                lse.data_ptr(), B, Hq, Hkv, N, d, int(bool(causal)), float(scale),
                                _dtype_code(q), _stream_handle(stream))
+    _raise(rc)
+    return out, lse
+
+
+def quantize_fp8(q, k, v, signs=None, stream=None) -> dict:
+    """e4m3 codes and scales of q, k, v (16-bit, d = 128) for forward_fp8 (see fa.h).
+
+    signs: int8 CUDA tensor of d values +1/-1 (the random signs of the Hadamard
+    rotation of q and k), or None for no rotation.  Returns a dict with q8, k8
+    (uint8 [B,H,N,d]), v8t (uint8 [B,Hkv,d,Np], V transposed), q_scale, k_scale
+    (float32 [B,H,ceil(N/128)]) and v_scale (float32 [B,Hkv,d]).
+    """
+    B, Hq, N, d = q.shape
+    Hkv = k.shape[1]
+    _check(q, "q", (B, Hq, N, d), q.dtype)
+    _check(k, "k", (B, Hkv, N, d), q.dtype)
+    _check(v, "v", (B, Hkv, N, d), q.dtype)
+    if signs is not None:
+        _check(signs, "signs", (d,), torch.int8)
+    lib = load()
+    Np = int(lib.fa_fp8_vt_stride(N))
+    T = (N + 127) // 128
+    dev = q.device
+    out = dict(q8=torch.empty((B, Hq, N, d), dtype=torch.uint8, device=dev),
+               k8=torch.empty((B, Hkv, N, d), dtype=torch.uint8, device=dev),
+               v8t=torch.empty((B, Hkv, d, Np), dtype=torch.uint8, device=dev),
+               q_scale=torch.empty((B, Hq, T), dtype=torch.float32, device=dev),
+               k_scale=torch.empty((B, Hkv, T), dtype=torch.float32, device=dev),
+               v_scale=torch.empty((B, Hkv, d), dtype=torch.float32, device=dev))
+    rc = lib.fa_quantize_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                             None if signs is None else signs.data_ptr(),
+                             *(out[n].data_ptr() for n in ("q8", "k8", "v8t", "q_scale", "k_scale",
+                                                           "v_scale")),
+                             B, Hq, Hkv, N, d, _dtype_code(q), _stream_handle(stream))
+    _raise(rc)
+    return out
+
+
+def forward_fp8(fp8: dict, causal: bool = False, scale: float | None = None, out=None, lse=None,
+                stream=None):
+    """Attention over e4m3 inputs from quantize_fp8 (see fa.h); O in bfloat16.
+
+    Returns (o [B,Hq,N,d] bfloat16, lse [B,Hq,N] float32).
+    """
+    q8, k8, v8t = fp8["q8"], fp8["k8"], fp8["v8t"]
+    B, Hq, N, d = q8.shape
+    Hkv = k8.shape[1]
+    Np = int(load().fa_fp8_vt_stride(N))
+    T = (N + 127) // 128
+    _check(q8, "q8", (B, Hq, N, d), torch.uint8)
+    _check(k8, "k8", (B, Hkv, N, d), torch.uint8)
+    _check(v8t, "v8t", (B, Hkv, d, Np), torch.uint8)
+    _check(fp8["q_scale"], "q_scale", (B, Hq, T), torch.float32)
+    _check(fp8["k_scale"], "k_scale", (B, Hkv, T), torch.float32)
+    _check(fp8["v_scale"], "v_scale", (B, Hkv, d), torch.float32)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    out = torch.empty((B, Hq, N, d), dtype=torch.bfloat16, device=q8.device) if out is None else out
+    lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q8.device) if lse is None else lse
+    _check(out, "out", (B, Hq, N, d), torch.bfloat16)
+    _check(lse, "lse", (B, Hq, N), torch.float32)
+    rc = load().fa_forward_fp8(q8.data_ptr(), k8.data_ptr(), v8t.data_ptr(),
+                               fp8["q_scale"].data_ptr(), fp8["k_scale"].data_ptr(),
+                               fp8["v_scale"].data_ptr(), out.data_ptr(), lse.data_ptr(), B, Hq, Hkv,
+                               N, d, int(bool(causal)), float(scale), _stream_handle(stream))
     _raise(rc)
     return out, lse
 

@@ -125,6 +125,23 @@ int encode_tile_map(CUtensorMap* map, const void* base, int heads, int N, int d,
   return FA_OK;
 }
 
+// Byte tensor [heads][rows][cols] (e4m3 codes), box {128, 128, 1}, 128-byte swizzle:
+// one box is a 128 x 128-byte tile, a single swizzle atom wide.
+int encode_u8_map(CUtensorMap* map, const void* base, int heads, int rows, int cols,
+                  const char* name) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(heads)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols),
+                           static_cast<cuuint64_t>(rows) * static_cast<cuuint64_t>(cols)};
+  cuuint32_t box[3] = {128, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides,
+                        box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed: %d", name, (int)r);
+  return FA_OK;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int check_common(int B, int Hq, int Hkv, int N, int d, float scale, int dtype) {
@@ -326,6 +343,70 @@ int fa_forward_splitkv(const void* q, const void* k, const void* v, void* o, flo
   a.err = st->err_word;
   cudaError_t e = fa::launch_decode(s, a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(FA_ERR_CUDA, "split-KV forward launch: %s", cudaGetErrorString(e));
+  return FA_OK;
+}
+
+int fa_fp8_vt_stride(int N) { return N <= 0 ? 0 : (N + 15) / 16 * 16; }
+
+int fa_forward_fp8(const void* q8, const void* k8, const void* v8t, const float* q_scale,
+                   const float* k_scale, const float* v_scale, void* o, float* lse, int B, int Hq,
+                   int Hkv, int N, int d, int causal, float scale, void* stream) {
+  t_last_error.clear();
+  if (!q8 || !k8 || !v8t || !q_scale || !k_scale || !v_scale || !o || !lse)
+    return fail(FA_ERR_INVALID, "null tensor pointer");
+  int rc = check_common(B, Hq, Hkv, N, d, scale, FA_DTYPE_BF16);
+  if (rc) return rc;
+  if (d != 128) return fail(FA_ERR_UNSUPPORTED, "FP8 path: head dimension d=%d (supported: 128)", d);
+  const void* ptrs[] = {q8, k8, v8t, q_scale, k_scale, v_scale, o, lse};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return fail(FA_ERR_UNSUPPORTED, "all tensor pointers must be 16-byte aligned");
+  DeviceState* st = nullptr;
+  if ((rc = get_device_state(&st))) return rc;
+  fa::AttnShape s{B, Hq, Hkv, N, d, causal ? 1 : 0, scale, 1, 0};
+  fa::FwdArgs a{};
+  if ((rc = encode_u8_map(&a.tm_q, q8, B * Hq, N, d, "q8"))) return rc;
+  if ((rc = encode_u8_map(&a.tm_k, k8, B * Hkv, N, d, "k8"))) return rc;
+  if ((rc = encode_u8_map(&a.tm_v, v8t, B * Hkv, d, fa_fp8_vt_stride(N), "v8t"))) return rc;
+  a.o = o;
+  a.lse = lse;
+  a.err = st->err_word;
+  a.q_scale = q_scale;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
+  cudaError_t e = fa::launch_forward_fp8(s, a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(FA_ERR_CUDA, "FP8 forward launch: %s", cudaGetErrorString(e));
+  return FA_OK;
+}
+
+int fa_quantize_fp8(const void* q, const void* k, const void* v, const signed char* signs, void* q8,
+                    void* k8, void* v8t, float* q_scale, float* k_scale, float* v_scale, int B,
+                    int Hq, int Hkv, int N, int d, int dtype, void* stream) {
+  t_last_error.clear();
+  if (!q || !k || !v || !q8 || !k8 || !v8t || !q_scale || !k_scale || !v_scale)
+    return fail(FA_ERR_INVALID, "null tensor pointer");
+  int rc = check_common(B, Hq, Hkv, N, d, 1.0f, dtype);
+  if (rc) return rc;
+  if (d != 128) return fail(FA_ERR_UNSUPPORTED, "FP8 path: head dimension d=%d (supported: 128)", d);
+  const void* ptrs[] = {q, k, v, q8, k8, v8t, q_scale, k_scale, v_scale};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return fail(FA_ERR_UNSUPPORTED, "all tensor pointers must be 16-byte aligned");
+  DeviceState* st = nullptr;
+  if ((rc = get_device_state(&st))) return rc;
+  fa::AttnShape s{B, Hq, Hkv, N, d, 0, 1.0f, dtype == FA_DTYPE_BF16, 0};
+  fa::Fp8QuantArgs a{};
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.signs = signs;
+  a.q8 = static_cast<uint8_t*>(q8);
+  a.k8 = static_cast<uint8_t*>(k8);
+  a.v8t = static_cast<uint8_t*>(v8t);
+  a.q_scale = q_scale;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
+  a.Np = fa_fp8_vt_stride(N);
+  cudaError_t e = fa::launch_quantize_fp8(s, a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(FA_ERR_CUDA, "FP8 quantization launch: %s", cudaGetErrorString(e));
   return FA_OK;
 }
 

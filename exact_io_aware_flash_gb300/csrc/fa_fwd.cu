@@ -36,6 +36,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 namespace fa {
 namespace {
@@ -57,9 +58,9 @@ constexpr int kKStages = 3;
 constexpr int kVStages = 2;
 constexpr int kConsumerWarps = 10;  // 8 softmax warps + 2 MMA issuer warps read each item
 
-template <int D>
+template <int D, int ELT>
 struct FwdSmem {
-  static constexpr int kTile = kBM * D * 2;  // bytes of one 128 x D 16-bit tile
+  static constexpr int kTile = kBM * D * ELT;  // bytes of one 128 x D tile of ELT-byte elements
   static constexpr int kQ = 0;               // 2 query tiles
   static constexpr int kK = kQ + 2 * kTile;  // K ring, kKStages
   static constexpr int kV = kK + kKStages * kTile;  // V ring, kVStages
@@ -154,14 +155,25 @@ __device__ __forceinline__ FwdItem decode_item(int item, int heads, int head_gro
 // reaches, and the window's lower edge is masked element-wise ("Flash
 // Attention" (aiwiki.ai), sections "Features" and "Block-sparse
 // FlashAttention": blocks a mask leaves empty are skipped).
-template <int D, bool BF16, bool WIN>
+// F8: e4m3 inputs ("FlashAttention Primer", section "FlashAttention-3: Hopper
+// asynchrony and FP8": block-quantized FP8 operands).  Q and K arrive as codes
+// with one scale per 128-row block (q_scale, k_scale), V as transposed codes
+// [d][keys] with one scale per channel (v_scale); both products run as
+// kind::f8f6f4 MMAs (twice the 16-bit rate), P is rounded to e4m3 for P V, the
+// block scales enter each round's exponent factor and the channel scales the
+// epilogue.  O is written in bfloat16.
+template <int D, bool BF16, bool WIN, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, void* __restrict__ out,
                   float* __restrict__ lse_out, int heads, int head_group, int Hq, int Hkv, int N,
-                  int causal, int window, float scale_log2, int* err) {
-  using L = FwdSmem<D>;
-  constexpr int kAtoms = D / 64;
+                  int causal, int window, float scale_log2, const float* __restrict__ q_scale,
+                  const float* __restrict__ k_scale, const float* __restrict__ v_scale, int* err) {
+  static_assert(!F8 || (D == 128 && BF16 && !WIN), "e4m3 path: d = 128, bfloat16 output, no window");
+  constexpr int kElt = F8 ? 1 : 2;
+  using L = FwdSmem<D, kElt>;
+  constexpr int kAtoms = D * kElt / 128;  // 128-byte-wide atoms per tile row
+  constexpr int kAtomCols = 128 / kElt;   // elements per atom row
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -241,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_expect_tx(&bar[BQFULL + X], L::kTile);
           for (int a = 0; a < kAtoms; ++a)
             tma_load_3d(smem + L::kQ + X * L::kTile + a * kAtomBytes, &tm_q, &bar[BQFULL + X],
-                        a * 64, (X ? it.tB : it.tA) * kBM, it.bh, pol_q);
+                        a * kAtomCols, (X ? it.tB : it.tA) * kBM, it.bh, pol_q);
           qpend[X] = quse[X] & 1;
           ++quse[X];
         }
@@ -252,13 +264,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_expect_tx(&bar[BKFULL + sk], L::kTile);
           for (int a = 0; a < kAtoms; ++a)
             tma_load_3d(smem + L::kK + sk * L::kTile + a * kAtomBytes, &tm_k, &bar[BKFULL + sk],
-                        a * 64, (it.loA + j) * kBN, it.kvh, pol_kv);
+                        a * kAtomCols, (it.loA + j) * kBN, it.kvh, pol_kv);
           kdone = kv + 1;
           if (!(ok = mbar_wait(&bar[BVEMPTY + sv], ((kv / kVStages) & 1) ^ 1, abort_flag, err))) break;
           mbar_expect_tx(&bar[BVFULL + sv], L::kTile);
-          for (int a = 0; a < kAtoms; ++a)
-            tma_load_3d(smem + L::kV + sv * L::kTile + a * kAtomBytes, &tm_v, &bar[BVFULL + sv],
-                        a * 64, (it.loA + j) * kBN, it.kvh, pol_kv);
+          if constexpr (F8) {  // transposed codes: box of d rows x 128 keys
+            tma_load_3d(smem + L::kV + sv * L::kTile, &tm_v, &bar[BVFULL + sv], (it.loA + j) * kBN, 0,
+                        it.kvh, pol_kv);
+          } else {
+            for (int a = 0; a < kAtoms; ++a)
+              tma_load_3d(smem + L::kV + sv * L::kTile + a * kAtomBytes, &tm_v, &bar[BVFULL + sv],
+                          a * 64, (it.loA + j) * kBN, it.kvh, pol_kv);
+          }
           vdone = kv + 1;
         }
         if (!ok) break;
@@ -299,8 +316,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // accumulator).  K_j and V_j are released when both tiles are done with
     // them: the empty barriers count one arrival per issuer.
     const int X = warp - 9;
-    constexpr uint32_t kIdS = idesc_f16(kBM, kBN, BF16, false, false);
-    constexpr uint32_t kIdO = idesc_f16(kBM, D, BF16, false, true);
+    constexpr uint32_t kIdS = F8 ? idesc_e4m3(kBM, kBN) : idesc_f16(kBM, kBN, BF16, false, false);
+    constexpr uint32_t kIdO = F8 ? idesc_e4m3(kBM, D) : idesc_f16(kBM, D, BF16, false, true);
     const uint32_t qa = smem_u32(smem + L::kQ) + X * L::kTile;
     const uint32_t sk = smem_u32(smem + L::kK);
     const uint32_t sv = smem_u32(smem + L::kV);
@@ -310,9 +327,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto issue_s = [&](int stk) {  // S_X = Q_X K_j^T
       const uint32_t ka = sk + stk * L::kTile;
 #pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks) {
+      for (int ks = 0; ks < D * kElt / 32; ++ks) {  // 32 bytes of K per instruction
         const uint32_t off = (ks >> 2) * kAtomBytes + (ks & 3) * 32;
-        mma_ss(tS, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), kIdS, ks > 0);
+        if constexpr (F8)
+          mma_ss_e4m3(tS, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), kIdS, ks > 0);
+        else
+          mma_ss(tS, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), kIdS, ks > 0);
       }
       mma_commit(&bar[BSFULL + X]);
       mma_commit(&bar[BKEMPTY + stk]);
@@ -320,9 +340,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto issue_pv = [&](int stv, bool first) {
       const uint32_t va = sv + stv * L::kTile;
 #pragma unroll
-      for (int ks = 0; ks < kBN / 16; ++ks)
-        mma_ts(tO, tS + ks * 8, sdesc_sw128(va + ks * 2048, kAtomBytes, 1024), kIdO,
-               (!first || ks > 0) ? 1u : 0u);
+      for (int ks = 0; ks < kBN * kElt / 32; ++ks) {
+        // P: 32 bytes of keys = 8 TMEM columns per instruction.  V: MN-major
+        // 16-bit tile, or (e4m3) the transposed codes as a K-major operand.
+        if constexpr (F8)
+          mma_ts_e4m3(tO, tS + ks * 8, sdesc_sw128(va + ks * 32, 16, 1024), kIdO,
+                      (!first || ks > 0) ? 1u : 0u);
+        else
+          mma_ts(tO, tS + ks * 8, sdesc_sw128(va + ks * 2048, kAtomBytes, 1024), kIdO,
+                 (!first || ks > 0) ? 1u : 0u);
+      }
       mma_commit(&bar[BODONE + X]);
       mma_commit(&bar[BVEMPTY + stv]);
     };
@@ -414,7 +441,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tmem + lane_off + X * 128;
     const uint32_t tO = tmem + lane_off + 256 + X * 128;
     const bool pos_scale = scale_log2 > 0.f;
-    const float sfac = pos_scale ? scale_log2 : 1.0f;
     int xs = 0;           // softmax rounds of this tile so far over all items
     int tokens = 0;       // turns handed to this tile so far
     int prev_nA = 0, prev_nB = 0;  // rounds of each tile in the previous item (0: none yet)
@@ -433,6 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int t = X ? it.tB : it.tA;
       const int nX = X ? it.nB : it.nA;
       const int loX = X ? it.loB : it.loA;  // key tile of round 0
+      const float qsc = F8 ? q_scale[static_cast<size_t>(it.bh) * T + t] : 1.f;
       const int m = it.nA < it.nB ? it.nA : it.nB;  // rounds both tiles have
       const int q = t * kBM + r;
       float m_run = -INFINITY;
@@ -472,13 +499,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         reg_fence<kBN>(x);
         const int kbase = (loX + j) * kBN;
         const bool diag = causal && (loX + j == t);
-        // Scores stay raw when scale > 0 (the exponent is then one FFMA,
-        // s * scale*log2(e) - m, and the row maximum of raw scores times the
-        // positive factor is the maximum of the scaled scores); for scale <= 0
-        // they are scaled first and the factor below is 1.
-        if (!pos_scale) {
+        // The factor from raw scores to the exp2 domain: scale*log2(e), times the
+        // query and key blocks' dequantization scales for e4m3 inputs.
+        float fac = scale_log2;
+        bool pos = pos_scale;
+        if constexpr (F8) {
+          fac = scale_log2 * (qsc * k_scale[static_cast<size_t>(it.kvh) * T + loX + j]);
+          pos = fac > 0.f;
+        }
+        const float sfac_r = pos ? fac : 1.0f;
+        // Scores stay raw when the factor is positive (the exponent is then one
+        // FFMA, s * factor - m, and the row maximum of raw scores times the
+        // positive factor is the maximum of the scaled scores); otherwise they
+        // are scaled first and the factor below is 1.
+        if (!pos) {
 #pragma unroll
-          for (int c = 0; c < kBN; ++c) x[c] = __float_as_uint(__uint_as_float(x[c]) * scale_log2);
+          for (int c = 0; c < kBN; ++c) x[c] = __float_as_uint(__uint_as_float(x[c]) * fac);
         }
         if (diag || kbase + kBN > N) {
           int lim = N - kbase;
@@ -508,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           m8[u] = fmaxf(m, __uint_as_float(x[u + 120]));
         }
         const float mx =
-            fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7])) * sfac;
+            fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7])) * sfac_r;
         // Conditional rescale: keep the stale maximum unless it grew by more than 8
         // (p <= 2^8 then); the decision is warp-uniform because TMEM access is.
         float alpha = 1.0f;
@@ -527,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // whose keys so far are all masked has m_run = -inf; its exponents are
         // taken against 0 (all p = 0), and its next round rescales by 0.
         const float m_use = (WIN && m_run == -INFINITY) ? 0.f : m_run;
-        const uint64_t sfac2 = f2_pack(sfac, sfac);
+        const uint64_t sfac2 = f2_pack(sfac_r, sfac_r);
         const uint64_t negm2 = f2_pack(-m_use, -m_use);
         uint64_t rs2[2] = {0ull, 0ull};
 #pragma unroll
@@ -542,9 +578,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float p0 = ex2_approx(a0);
             const float p1 = ex2_approx(a1);
             rs2[e & 1] = f2_add(rs2[e & 1], f2_pack(p0, p1));
-            pk[e] = pack2<BF16>(p0, p1);
+            if constexpr (F8) {  // four e4m3 per column, the lowest key in the lowest byte
+              const uint32_t h2 = __nv_cvt_float2_to_fp8x2(make_float2(p0, p1), __NV_SATFINITE, __NV_E4M3);
+              pk[e >> 1] = (e & 1) ? (pk[e >> 1] | (h2 << 16)) : h2;
+            } else {
+              pk[e] = pack2<BF16>(p0, p1);
+            }
           }
-          tmem_st16(tS + c / 2, pk);
+          if constexpr (F8)
+            tmem_st8(tS + c / 4, pk);
+          else
+            tmem_st16(tS + c / 2, pk);
         }
         float r0, r1, r2, r3;
         f2_unpack(rs2[0], r0, r1);
@@ -587,9 +631,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_wait();
           reg_fence<32>(o);
           uint32_t pk[16];
+          if constexpr (F8) {  // V's channel scales
+            const float* vsc = v_scale + static_cast<size_t>(it.kvh) * D + c;
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            pk[e] = pack2<BF16>(__uint_as_float(o[2 * e]) * inv_l, __uint_as_float(o[2 * e + 1]) * inv_l);
+            for (int e = 0; e < 16; ++e)
+              pk[e] = pack2<BF16>(__uint_as_float(o[2 * e]) * (inv_l * vsc[2 * e]),
+                                  __uint_as_float(o[2 * e + 1]) * (inv_l * vsc[2 * e + 1]));
+          } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              pk[e] = pack2<BF16>(__uint_as_float(o[2 * e]) * inv_l, __uint_as_float(o[2 * e + 1]) * inv_l);
+          }
           if (valid) {
             uint4* dst = reinterpret_cast<uint4*>(orow + c);
 #pragma unroll
@@ -616,12 +668,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, bool BF16, bool WIN>
+template <int D, bool BF16, bool WIN, bool F8 = false>
 cudaError_t launch_fwd_t(const AttnShape& s, const FwdArgs& a, cudaStream_t stream) {
-  auto kern = fa_fwd_kernel<D, BF16, WIN>;
-  constexpr int smem = FwdSmem<D>::kAlloc;
+  auto kern = fa_fwd_kernel<D, BF16, WIN, F8>;
+  constexpr int smem = FwdSmem<D, F8 ? 1 : 2>::kAlloc;
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), smem,
-                                (WIN ? 4 : 0) + (D == 64 ? 0 : 2) + (BF16 ? 1 : 0));
+                                F8 ? 28 : (WIN ? 4 : 0) + (D == 64 ? 0 : 2) + (BF16 ? 1 : 0));
   if (e != cudaSuccess) return e;
   const int T = (s.N + kBM - 1) / kBM;
   const int pairs = (T + 1) / 2;
@@ -634,14 +686,19 @@ cudaError_t launch_fwd_t(const AttnShape& s, const FwdArgs& a, cudaStream_t stre
   hg = hg < 1 ? 1 : (hg > 64 ? 64 : hg);
   kern<<<grid, kThreads, smem, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.o, a.lse, s.B * s.Hq,
                                          static_cast<int>(hg), s.Hq, s.Hkv, s.N, s.causal,
-                                         s.window, scale_log2, a.err);
+                                         s.window, scale_log2, a.q_scale, a.k_scale, a.v_scale,
+                                         a.err);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 size_t forward_smem_bytes(int d) {
-  return d == 64 ? FwdSmem<64>::kAlloc : FwdSmem<128>::kAlloc;
+  return d == 64 ? FwdSmem<64, 2>::kAlloc : FwdSmem<128, 2>::kAlloc;
+}
+
+cudaError_t launch_forward_fp8(const AttnShape& s, const FwdArgs& a, cudaStream_t stream) {
+  return launch_fwd_t<128, true, false, true>(s, a, stream);
 }
 
 cudaError_t launch_forward(const AttnShape& s, const FwdArgs& a, cudaStream_t stream) {

@@ -25,6 +25,11 @@ struct FwdArgs {
   void* o;
   float* lse;
   int* err;
+  // e4m3 inputs only (launch_forward_fp8): dequantization scales per 128-row
+  // block of Q [B*Hq][T] and K [B*Hkv][T], and per channel of V [B*Hkv][d]
+  const float* q_scale;
+  const float* k_scale;
+  const float* v_scale;
 };
 
 struct BwdArgs {
@@ -58,10 +63,31 @@ struct DecodeArgs {
   int* err;
 };
 
+// FP8 (e4m3) quantization of 16-bit Q, K, V (d = 128): codes q8 [B*Hq][N][d],
+// k8 [B*Hkv][N][d], v8t [B*Hkv][d][Np]; scales per 128-row block (Q, K) and per
+// channel (V).  signs: d bytes of +1/-1 on the device, or null for no rotation.
+struct Fp8QuantArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const signed char* signs;
+  uint8_t* q8;
+  uint8_t* k8;
+  uint8_t* v8t;
+  float* q_scale;  // [B*Hq][ceil(N/128)]
+  float* k_scale;  // [B*Hkv][ceil(N/128)]
+  float* v_scale;  // [B*Hkv][d]
+  int Np;          // row stride of v8t in bytes: N rounded up to a multiple of 16
+};
+
 // Each returns cudaSuccess or the launch error.  `stream` is the caller's.
 cudaError_t launch_forward(const AttnShape& s, const FwdArgs& a, cudaStream_t stream);
+// e4m3 codes (tm_q, tm_k over [B*H][N][d] bytes; tm_v over the transposed V
+// codes [B*Hkv][d][Np]), d = 128, bfloat16 O.
+cudaError_t launch_forward_fp8(const AttnShape& s, const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_backward(const AttnShape& s, const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_decode(const AttnShape& s, const DecodeArgs& a, cudaStream_t stream);
+cudaError_t launch_quantize_fp8(const AttnShape& s, const Fp8QuantArgs& a, cudaStream_t stream);
 
 // Raises a kernel's dynamic shared-memory limit to `bytes` once per device
 // (cudaFuncSetAttribute is a host round trip; calls after the first are free).

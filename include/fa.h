@@ -101,6 +101,47 @@ FA_API int fa_forward_window(const void* q, const void* k, const void* v, void* 
                              int dtype, void* stream);
 
 /*
+ * FP8 (e4m3) forward ("FlashAttention Primer", section "FlashAttention-3: Hopper
+ * asynchrony and FP8": block quantization, and an incoherent rotation applied
+ * before quantization that lowers the FP8 error; "Flash Attention" (aiwiki.ai),
+ * section "FlashAttention-3": the rotation is random signs and a Hadamard
+ * transform, applied to queries and keys alike so that their dot products are
+ * kept).  d = 128 only.
+ *
+ * fa_quantize_fp8: q, k, v (16-bit, [B,H,N,d] as fa_forward, element type
+ * dtype) -> e4m3 codes and fp32 dequantization scales:
+ *   q8 [B,Hq,N,d], k8 [B,Hkv,N,d]: row y = (x * s) H_d (s = signs, +1/-1 per
+ *     channel, d bytes in device memory; H_d the Sylvester Hadamard matrix, entries
+ *     +-1), then per 128-row block of a head: amax = max |y|, code =
+ *     e4m3(y * 448/amax) (round to nearest even, saturating);
+ *   q_scale [B,Hq,ceil(N/128)], k_scale [B,Hkv,ceil(N/128)]: amax / (448 sqrt(d)),
+ *     so that code * scale is the orthogonally rotated input (x * s) H_d / sqrt(d);
+ *   v8t [B,Hkv,d,Np], Np = fa_fp8_vt_stride(N): V transposed (channel-major),
+ *     code = e4m3(v * 448/amax_c) with one amax per (head, channel) over all N
+ *     rows, keys N..Np-1 zero; v_scale [B,Hkv,d] = amax_c / 448.
+ * signs may be NULL: no rotation, and q_scale, k_scale = amax / 448.  Every fp32
+ * step that decides a code is exactly rounded in a fixed order, so the codes are
+ * reproducible bit for bit.
+ *
+ * fa_forward_fp8: attention over the dequantized inputs -- O = softmax(scale *
+ * Qh Kh^T) Vh with Qh = code * q_scale per block etc. -- on e4m3 tensor cores,
+ * the probabilities rounded to e4m3 for the P V product; O is written in
+ * bfloat16 [B,Hq,N,d], lse (fp32 [B,Hq,N]) as in fa_forward.  The rotation
+ * leaves Q K^T unchanged, so `scale` is the usual one (1/sqrt(d)).
+ *
+ * Both allocate nothing, run asynchronously on `stream`, and return the
+ * fa_forward error codes (FA_ERR_UNSUPPORTED for d != 128).
+ */
+FA_API int fa_fp8_vt_stride(int N);
+FA_API int fa_quantize_fp8(const void* q, const void* k, const void* v, const signed char* signs,
+                           void* q8, void* k8, void* v8t, float* q_scale, float* k_scale,
+                           float* v_scale, int B, int Hq, int Hkv, int N, int d, int dtype,
+                           void* stream);
+FA_API int fa_forward_fp8(const void* q8, const void* k8, const void* v8t, const float* q_scale,
+                          const float* k_scale, const float* v_scale, void* o, float* lse, int B,
+                          int Hq, int Hkv, int N, int d, int causal, float scale, void* stream);
+
+/*
  * Split-KV forward for decoding: a few query rows against a long key sequence
  * ("Flash Attention" (aiwiki.ai), section "Flash-Decoding": split the keys
  * into chunks, attend to each chunk with its own log-sum-exp, combine).

@@ -479,10 +479,19 @@ int oracle_fp8_quantize_qk(const float* x, const signed char* signs, int heads, 
         return ORACLE_EINVAL;
     const int T = (N + 127) / 128;
     const float cfac = signs ? (float)(1.0 / (448.0 * sqrt((double)d))) : (float)(1.0 / 448.0);
+    int failed = 0;
+#pragma omp parallel
+    {
     float* y = (float*)malloc(sizeof(float) * (size_t)128 * d);
-    if (!y) return ORACLE_ENOMEM;
-    for (int h = 0; h < heads; ++h)
-        for (int t = 0; t < T; ++t) {
+    if (!y) {
+#pragma omp atomic write
+        failed = 1;
+    }
+    /* blocks are independent: the same result for any thread count */
+#pragma omp for schedule(dynamic, 1)
+    for (long ht = 0; ht < (long)heads * T; ++ht) {
+            if (!y) continue;
+            const int h = (int)(ht / T), t = (int)(ht % T);
             const int r0 = t * 128, r1 = (r0 + 128 < N) ? r0 + 128 : N;
             float amax = 0.f;
             for (int r = r0; r < r1; ++r) {
@@ -499,9 +508,10 @@ int oracle_fp8_quantize_qk(const float* x, const signed char* signs, int heads, 
                 for (int c = 0; c < d; ++c)
                     codes[((size_t)h * N + r) * d + c] =
                         (unsigned char)oracle_e4m3_encode(y[(size_t)(r - r0) * d + c] * f);
-        }
+    }
     free(y);
-    return ORACLE_OK;
+    }
+    return failed ? ORACLE_ENOMEM : ORACLE_OK;
 }
 
 /* V: v [heads, N, d].  One scale per (head, channel):
@@ -512,8 +522,10 @@ int oracle_fp8_quantize_v(const float* v, int heads, int N, int d, unsigned char
                           float* scales) {
     if (heads <= 0 || N <= 0 || d <= 0 || !v || !codes || !scales) return ORACLE_EINVAL;
     const float cfac = (float)(1.0 / 448.0);
-    for (int h = 0; h < heads; ++h)
-        for (int c = 0; c < d; ++c) {
+    /* (head, channel) pairs are independent: the same result for any thread count */
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long hc = 0; hc < (long)heads * d; ++hc) {
+            const int h = (int)(hc / d), c = (int)(hc % d);
             float amax = 0.f;
             for (int r = 0; r < N; ++r) {
                 const float a = fabsf(v[((size_t)h * N + r) * d + c]);
@@ -525,13 +537,14 @@ int oracle_fp8_quantize_v(const float* v, int heads, int N, int d, unsigned char
                 const size_t e = ((size_t)h * N + r) * d + c;
                 codes[e] = (unsigned char)oracle_e4m3_encode(v[e] * f);
             }
-        }
+    }
     return ORACLE_OK;
 }
 
 /* Element-wise front ends of the two functions above, for arrays. */
 int oracle_e4m3_encode_array(const float* x, unsigned char* out, long n) {
     if (n < 0 || (n > 0 && (!x || !out))) return ORACLE_EINVAL;
+#pragma omp parallel for schedule(static)
     for (long i = 0; i < n; ++i) out[i] = (unsigned char)oracle_e4m3_encode(x[i]);
     return ORACLE_OK;
 }

@@ -115,3 +115,20 @@ def test_window_entry_points_validate_before_device_work(lib):
     assert lib.fa_backward_window(fake, fake, fake, fake, fake, fake, fake, fake, fake, fake, 16,
                                   1, 1, 1, 8, 64, 4, 1.0, 0, null) == 1
     assert b"workspace" in lib.fa_last_error()
+
+
+def test_fp8_entry_points_validate_before_device_work(lib):
+    fake = ctypes.c_void_p(4096)
+    null = ctypes.c_void_p(0)
+    assert lib.fa_fp8_vt_stride(1) == 16 and lib.fa_fp8_vt_stride(300) == 304
+    assert lib.fa_fp8_vt_stride(0) == 0
+    # d must be 128
+    assert lib.fa_quantize_fp8(fake, fake, fake, null, fake, fake, fake, fake, fake, fake,
+                               1, 1, 1, 8, 64, 1, null) == 2
+    assert lib.fa_forward_fp8(fake, fake, fake, fake, fake, fake, fake, fake, 1, 1, 1, 8, 64, 0, 1.0,
+                              null) == 2
+    # null tensor, GQA divisibility
+    assert lib.fa_quantize_fp8(null, fake, fake, null, fake, fake, fake, fake, fake, fake,
+                               1, 1, 1, 8, 128, 1, null) == 1
+    assert lib.fa_forward_fp8(fake, fake, fake, fake, fake, fake, fake, fake, 1, 3, 2, 8, 128, 0, 1.0,
+                              null) == 1
