@@ -579,6 +579,32 @@ def workload_table(dev, peaks):
         bwd[f"N{N}"] = e
         del q, k, v, dO, o, lse, ws, dq, dk, dv
     out["backward_sweep"] = bwd
+    # FP8 (e4m3) forward on the two large forward workloads' shapes: quantization
+    # (rotation + block scales, HBM-bound) and attention over the codes
+    from exact_io_aware_flash_gb300 import forward_fp8, quantize_fp8
+    fp8_peak = 2.0 * burst  # e4m3 dense rate = 2x the 16-bit rate (nominal ratio)
+    fp8 = {"peak_tflops": fp8_peak,
+           "peak_kind": "2 x the measured bf16 burst (nominal e4m3 : bf16 ratio 2:1)"}
+    for name in ("fwd_b4_h16_n4096_d128_bf16_causal", "gqa_fwd_b2_hq32_hkv8_n8192_d128_bf16_causal"):
+        s_ = WORKLOADS[name]["shape"]
+        inp = make_inputs(s_, "bf16", seed=WORKLOADS[name]["seed"], with_dO=False)
+        q, k, v = (inp[n].to(dev) for n in ("q", "k", "v"))
+        signs = torch.from_numpy(
+            __import__("numpy").random.default_rng(0).choice([-1, 1], s_.d).astype("int8")).to(dev)
+        codes = quantize_fp8(q, k, v, signs)
+        o = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
+        lse = torch.empty(s_.B, s_.Hq, s_.N, dtype=torch.float32, device=dev)
+        ms_q = _graph_time(lambda: quantize_fp8(q, k, v, signs), iters=10)
+        ms_f = _graph_time(lambda: forward_fp8(codes, causal=True, out=o, lse=lse))
+        fl = forward_flops(s_.B, s_.Hq, s_.N, s_.d, True)
+        qbytes = 2 * (q.numel() + k.numel() + v.numel()) + q.numel() + k.numel() + v.numel()
+        fp8[name.replace("_bf16", "_e4m3")] = {
+            "forward_ms": ms_f, "forward_tflops": fl / ms_f / 1e9,
+            "pct_of_fp8_peak": fl / ms_f / 1e9 / fp8_peak,
+            "quantize_ms": ms_q, "quantize_gbs": qbytes / ms_q / 1e6,
+            "quantize_frac_of_hbm": qbytes / ms_q / 1e6 / hbm}
+        del q, k, v, codes, o, lse
+    out["fp8_forward"] = fp8
     # sliding-window (local) causal attention, GQA 32/8, window 4096 over N = 16384
     from exact_io_aware_flash_gb300.flops import backward_flops_window, forward_flops_window
     B, Hq, Hkv, N, d, W = 1, 32, 8, 16384, 128, 4096
