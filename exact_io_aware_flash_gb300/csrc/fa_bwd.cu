@@ -95,6 +95,17 @@ __device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile, int ks) {
 __device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile, int ks) {
   return sdesc_sw128(tile + ks * 2048, kAtomBytes, 1024);
 }
+// The same descriptors from the k-step-0 descriptor d0 of the tile: only the
+// start-address field (bits 0-13, address >> 4) moves, and shared-memory
+// addresses stay below 2^18, so one add of a compile-time constant per
+// operand replaces the full encoding in the MMA-issuing thread, whose
+// instruction count is on every iteration's critical path.
+__device__ __forceinline__ uint64_t kmajor_step(uint64_t d0, int ks) {
+  return d0 + static_cast<uint64_t>(((ks >> 2) * kAtomBytes + (ks & 3) * 32) >> 4);
+}
+__device__ __forceinline__ uint64_t mnmajor_step(uint64_t d0, int ks) {
+  return d0 + static_cast<uint64_t>((ks * 2048) >> 4);
+}
 
 // TMEM row (D fp32 columns at taddr) * mul -> 16-bit row `row` of a 128-row
 // tile in shared memory, in the layout a 128-byte-swizzled TMA box expects:
@@ -286,22 +297,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_f16(kBlk, kBlk, BF16, false, false);  // S^T, dP^T
       constexpr uint32_t kIdKV = idesc_f16(kBlk, D, BF16, false, true);     // dV, dK
-      const uint32_t sk = smem_u32(smem + L::kK);
-      const uint32_t sv = smem_u32(smem + L::kV);
-      const uint32_t sq = smem_u32(smem + L::kQ);
-      const uint32_t sdo = smem_u32(smem + L::kdO);
+      constexpr uint64_t kStageStep = L::kTile >> 4;  // one stage further, in descriptor units
+      const uint64_t dk0 = kmajor_desc(smem_u32(smem + L::kK), 0);
+      const uint64_t dv0 = kmajor_desc(smem_u32(smem + L::kV), 0);
+      const uint64_t dq0 = kmajor_desc(smem_u32(smem + L::kQ), 0);
+      const uint64_t ddo0 = kmajor_desc(smem_u32(smem + L::kdO), 0);
+      const uint64_t mq0 = mnmajor_desc(smem_u32(smem + L::kQ), 0);
+      const uint64_t mdo0 = mnmajor_desc(smem_u32(smem + L::kdO), 0);
       auto issue_s = [&](int st) {  // S^T = K_j Q_i^T
-        const uint32_t qa = sq + st * L::kTile;
+        const uint64_t qd = dq0 + st * kStageStep;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks)
-          mma_ss(tmem + kColS, kmajor_desc(sk, ks), kmajor_desc(qa, ks), kIdS, ks > 0);
+          mma_ss(tmem + kColS, kmajor_step(dk0, ks), kmajor_step(qd, ks), kIdS, ks > 0);
         mma_commit(&bar[KB_SFULL]);
       };
       auto issue_dp = [&](int st) {  // dP^T = V_j dO_i^T
-        const uint32_t doa = sdo + st * L::kTile;
+        const uint64_t dd = ddo0 + st * kStageStep;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks)
-          mma_ss(tmem + kColDP, kmajor_desc(sv, ks), kmajor_desc(doa, ks), kIdS, ks > 0);
+          mma_ss(tmem + kColDP, kmajor_step(dv0, ks), kmajor_step(dd, ks), kIdS, ks > 0);
         mma_commit(&bar[KB_DPFULL]);
       };
       bool ok = mbar_wait(&bar[KB_KV], 0, abort_flag, err) &&
@@ -316,8 +330,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // P^T phase can start while this iteration's dS^T is still being computed.
       for (int it = 0; ok && it < n_it; ++it) {
         const int st = it & 1;
-        const uint32_t qa = sq + st * L::kTile;
-        const uint32_t doa = sdo + st * L::kTile;
+        const uint64_t qm = mq0 + st * kStageStep;
+        const uint64_t dom = mdo0 + st * kStageStep;
         const bool more = it + 1 < n_it;
         const int st1 = (it + 1) & 1;
         // dV += P^T dO_i   (P^T: 16-bit pairs over the first half of the S^T columns)
@@ -325,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < kBlk / 16; ++ks)
-          mma_ts(tmem + kColDV, tmem + kColS + ks * 8, mnmajor_desc(doa, ks), kIdKV,
+          mma_ts(tmem + kColDV, tmem + kColS + ks * 8, mnmajor_step(dom, ks), kIdKV,
                  (it > 0 || ks > 0) ? 1u : 0u);
         mma_commit(&bar[KB_DVDONE]);
         if (more) {
@@ -339,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < kBlk / 16; ++ks)
-          mma_ts(tmem + kColDK, tmem + kColDP + ks * 8, mnmajor_desc(qa, ks), kIdKV,
+          mma_ts(tmem + kColDK, tmem + kColDP + ks * 8, mnmajor_step(qm, ks), kIdKV,
                  (it > 0 || ks > 0) ? 1u : 0u);
         mma_commit(&bar[KB_DKDONE]);
         mma_commit(&bar[KB_QEMPTY + st]);
@@ -651,22 +665,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_f16(kBlk, kBlk, BF16, false, false);  // S, dP
       constexpr uint32_t kIdQ = idesc_f16(kBlk, D, BF16, false, true);      // dQ
-      const uint32_t sq = smem_u32(smem + L::kQ);
-      const uint32_t sdo = smem_u32(smem + L::kdO);
-      const uint32_t sk = smem_u32(smem + L::kK);
-      const uint32_t sv = smem_u32(smem + L::kV);
+      constexpr uint64_t kStageStep = L::kTile >> 4;  // one stage further, in descriptor units
+      const uint64_t dq0 = kmajor_desc(smem_u32(smem + L::kQ), 0);
+      const uint64_t ddo0 = kmajor_desc(smem_u32(smem + L::kdO), 0);
+      const uint64_t dk0 = kmajor_desc(smem_u32(smem + L::kK), 0);
+      const uint64_t dv0 = kmajor_desc(smem_u32(smem + L::kV), 0);
+      const uint64_t mk0 = mnmajor_desc(smem_u32(smem + L::kK), 0);
       auto issue_s = [&](int stk) {  // S = Q_i K_j^T
-        const uint32_t ka = sk + stk * L::kTile;
+        const uint64_t kd = dk0 + stk * kStageStep;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks)
-          mma_ss(tmem + kColS, kmajor_desc(sq, ks), kmajor_desc(ka, ks), kIdS, ks > 0);
+          mma_ss(tmem + kColS, kmajor_step(dq0, ks), kmajor_step(kd, ks), kIdS, ks > 0);
         mma_commit(&bar[QB_SFULL]);
       };
       auto issue_dp = [&](int stv) {  // dP = dO_i V_j^T; V_j is free again once this completes
-        const uint32_t va = sv + stv * L::kTile;
+        const uint64_t vd = dv0 + stv * kStageStep;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks)
-          mma_ss(tmem + kColDP, kmajor_desc(sdo, ks), kmajor_desc(va, ks), kIdS, ks > 0);
+          mma_ss(tmem + kColDP, kmajor_step(ddo0, ks), kmajor_step(vd, ks), kIdS, ks > 0);
         mma_commit(&bar[QB_DPFULL]);
         mma_commit(&bar[QB_VEMPTY + stv]);
       };
@@ -701,10 +717,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // dQ += dS K_j   (dS: 16-bit pairs in its own TMEM columns; K_j as an MN-major B)
         if (!(ok = mbar_wait(&bar[QB_DSREADY], jj & 1, abort_flag, err))) break;
         tc_fence_after();
-        const uint32_t ka = sk + stk * L::kTile;
+        const uint64_t km = mk0 + stk * kStageStep;
 #pragma unroll
         for (int ks = 0; ks < kBlk / 16; ++ks)
-          mma_ts(tmem + kColDQ, tmem + kColDS + ks * 8, mnmajor_desc(ka, ks), kIdQ,
+          mma_ts(tmem + kColDQ, tmem + kColDS + ks * 8, mnmajor_step(km, ks), kIdQ,
                  (jj > 0 || ks > 0) ? 1u : 0u);
         mma_commit(&bar[QB_DQDONE]);
         mma_commit(&bar[QB_KEMPTY + stk]);

@@ -324,30 +324,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tmem + X * 128;
     const uint32_t tO = tmem + 256 + X * 128;
 
+    // Descriptors: the k-step-0 encoding of each tile plus a compile-time
+    // offset of the start-address field (bits 0-13, address >> 4; shared
+    // addresses stay below 2^18), which keeps the issuing thread's per-MMA
+    // instruction count low.
+    constexpr uint64_t kStageStep = L::kTile >> 4;
+    const uint64_t dq0 = sdesc_sw128(qa, 16, 1024);
+    const uint64_t dk0 = sdesc_sw128(sk, 16, 1024);
+    const uint64_t dv0 = F8 ? sdesc_sw128(sv, 16, 1024) : sdesc_sw128(sv, kAtomBytes, 1024);
     auto issue_s = [&](int stk) {  // S_X = Q_X K_j^T
-      const uint32_t ka = sk + stk * L::kTile;
+      const uint64_t kd = dk0 + stk * kStageStep;
 #pragma unroll
       for (int ks = 0; ks < D * kElt / 32; ++ks) {  // 32 bytes of K per instruction
-        const uint32_t off = (ks >> 2) * kAtomBytes + (ks & 3) * 32;
+        const uint64_t off = static_cast<uint64_t>(((ks >> 2) * kAtomBytes + (ks & 3) * 32) >> 4);
         if constexpr (F8)
-          mma_ss_e4m3(tS, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), kIdS, ks > 0);
+          mma_ss_e4m3(tS, dq0 + off, kd + off, kIdS, ks > 0);
         else
-          mma_ss(tS, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), kIdS, ks > 0);
+          mma_ss(tS, dq0 + off, kd + off, kIdS, ks > 0);
       }
       mma_commit(&bar[BSFULL + X]);
       mma_commit(&bar[BKEMPTY + stk]);
     };
     auto issue_pv = [&](int stv, bool first) {
-      const uint32_t va = sv + stv * L::kTile;
+      const uint64_t vd = dv0 + stv * kStageStep;
 #pragma unroll
       for (int ks = 0; ks < kBN * kElt / 32; ++ks) {
         // P: 32 bytes of keys = 8 TMEM columns per instruction.  V: MN-major
         // 16-bit tile, or (e4m3) the transposed codes as a K-major operand.
         if constexpr (F8)
-          mma_ts_e4m3(tO, tS + ks * 8, sdesc_sw128(va + ks * 32, 16, 1024), kIdO,
+          mma_ts_e4m3(tO, tS + ks * 8, vd + static_cast<uint64_t>((ks * 32) >> 4), kIdO,
                       (!first || ks > 0) ? 1u : 0u);
         else
-          mma_ts(tO, tS + ks * 8, sdesc_sw128(va + ks * 2048, kAtomBytes, 1024), kIdO,
+          mma_ts(tO, tS + ks * 8, vd + static_cast<uint64_t>((ks * 2048) >> 4), kIdO,
                  (!first || ks > 0) ? 1u : 0u);
       }
       mma_commit(&bar[BODONE + X]);

@@ -81,6 +81,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Bounded wait for the phase of parity `parity` to complete.  Returns false if
 // the CTA-wide abort flag is raised or `limit_ns` expires (which raises both
 // the CTA flag and the global error word).  Never traps, never spins forever.
+//
+// The spin loop touches only shared memory and the global timer: a global
+// load here would hold the waiter for a whole memory latency (~700 clocks)
+// whenever the phase completes during it, and the wake-up latency of these
+// waits is on every pipeline's critical path.  The device error word (raised
+// by another CTA) is therefore polled only once a wait has lasted
+// kErrPollNs, far longer than any stage of a healthy pipeline.
+constexpr unsigned long long kErrPollNs = 20000ull;
+
 __device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity,
                                               volatile int* cta_abort, int* err_word,
                                               unsigned long long limit_ns) {
@@ -90,11 +99,12 @@ __device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity,
   while (!mbar_try_wait(bar, parity)) {
     if ((++spins & 63u) == 0) {
       if (*cta_abort) return false;
-      if (*(volatile int*)err_word != kDevErrNone) {
+      const unsigned long long dt = globaltimer_ns() - t0;
+      if (dt > kErrPollNs && *(volatile int*)err_word != kDevErrNone) {
         *cta_abort = 1;
         return false;
       }
-      if (globaltimer_ns() - t0 > limit_ns) {
+      if (dt > limit_ns) {
         *cta_abort = 1;
         atomicExch(err_word, kDevErrTimeout);
         return false;
@@ -106,24 +116,7 @@ __device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity,
 
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* cta_abort,
                                           int* err_word) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = globaltimer_ns();
-  uint32_t spins = 0;
-  while (!mbar_try_wait(bar, parity)) {
-    if ((++spins & 63u) == 0) {
-      if (*cta_abort) return false;
-      if (*(volatile int*)err_word != kDevErrNone) {
-        *cta_abort = 1;
-        return false;
-      }
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
-        *cta_abort = 1;
-        atomicExch(err_word, kDevErrTimeout);
-        return false;
-      }
-    }
-  }
-  return true;
+  return mbar_wait_for(bar, parity, cta_abort, err_word, kWaitLimitNs);
 }
 
 // ---------------------------------------------------------------- TMA
