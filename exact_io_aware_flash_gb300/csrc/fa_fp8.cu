@@ -66,19 +66,25 @@ __global__ void __launch_bounds__(kQkThreads)
 #pragma unroll
     for (int e = 0; e < 4; ++e) neg[e] = signs[4 * lane + e] < 0;
   }
+  // All 16 rows' loads are issued before any butterfly, so that they are in
+  // flight together (the kernel is bound by memory latency, not arithmetic).
+  uint2 raw[16];
+#pragma unroll
+  for (int rr = 0; rr < 16; ++rr) {
+    const int r = t * 128 + warp * 16 + rr;
+    raw[rr] = r < N ? *reinterpret_cast<const uint2*>(src + static_cast<size_t>(r) * D + 4 * lane)
+                    : make_uint2(0u, 0u);
+  }
   float y[16][4];
   float amax = 0.f;
 #pragma unroll
   for (int rr = 0; rr < 16; ++rr) {
-    const int r = t * 128 + warp * 16 + rr;
-    float a[4] = {0.f, 0.f, 0.f, 0.f};
-    if (r < N) {
-      const uint2 w = *reinterpret_cast<const uint2*>(src + static_cast<size_t>(r) * D + 4 * lane);
-      a[0] = to_f32<BF16>(static_cast<uint16_t>(w.x & 0xFFFFu));
-      a[1] = to_f32<BF16>(static_cast<uint16_t>(w.x >> 16));
-      a[2] = to_f32<BF16>(static_cast<uint16_t>(w.y & 0xFFFFu));
-      a[3] = to_f32<BF16>(static_cast<uint16_t>(w.y >> 16));
-    }
+    const uint2 w = raw[rr];
+    float a[4];
+    a[0] = to_f32<BF16>(static_cast<uint16_t>(w.x & 0xFFFFu));
+    a[1] = to_f32<BF16>(static_cast<uint16_t>(w.x >> 16));
+    a[2] = to_f32<BF16>(static_cast<uint16_t>(w.y & 0xFFFFu));
+    a[3] = to_f32<BF16>(static_cast<uint16_t>(w.y >> 16));
     if (signs) {
 #pragma unroll
       for (int e = 0; e < 4; ++e)
@@ -127,68 +133,109 @@ __global__ void __launch_bounds__(kQkThreads)
   }
 }
 
-// V, d = 128.  One CTA per (head, 16-channel slab): pass 1 takes the slab's channel
-// maxima over all N rows, pass 2 encodes and writes the codes transposed, row c of
-// the [d][Np] output holding channel c of every key (keys N .. Np-1 are zero).
+// V, d = 128, in three steps over (head, 128-row block) CTAs, every access
+// coalesced:
+//   1. channel maxima of the block, merged into v_scale by atomicMax on the
+//      fp32 bit patterns (non-negative floats order like their bits; the max
+//      does not depend on the order, so the result is deterministic);
+//   2. each block encodes with f_c = 448 / amax_c and writes its 128 keys of
+//      every channel into the transposed codes through a shared-memory tile;
+//   3. v_scale <- amax * fl32(1/448) in place.
+// v_scale must be zero before step 1 (the launcher clears it).
 constexpr int kVThreads = 256;
-constexpr int kVSlab = 16;
 
 template <bool BF16>
 __global__ void __launch_bounds__(kVThreads)
-    fa_fp8_v_kernel(const uint16_t* __restrict__ v, uint8_t* __restrict__ v8t,
-                    float* __restrict__ v_scale, int N, int Np, float cfac) {
+    fa_fp8_v_amax_kernel(const uint16_t* __restrict__ v, unsigned int* __restrict__ v_amax_bits,
+                         int N, int T) {
   constexpr int D = 128;
-  __shared__ float s_max[kVThreads / 32][kVSlab];
-  __shared__ float s_f[kVSlab];
-  const int head = blockIdx.x / (D / kVSlab);
-  const int c0 = (blockIdx.x % (D / kVSlab)) * kVSlab;
+  __shared__ float s_max[kVThreads / 32][D];
+  const int head = blockIdx.x / T;
+  const int t = blockIdx.x % T;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint16_t* src = v + static_cast<size_t>(head) * N * D + c0;
-  float m[kVSlab];
+  const uint16_t* src = v + static_cast<size_t>(head) * N * D;
+  uint2 raw[16];
 #pragma unroll
-  for (int c = 0; c < kVSlab; ++c) m[c] = 0.f;
-  for (int r = threadIdx.x; r < N; r += kVThreads) {
-    const uint4* p = reinterpret_cast<const uint4*>(src + static_cast<size_t>(r) * D);
-    const uint4 w0 = p[0], w1 = p[1];
-    const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+  for (int rr = 0; rr < 16; ++rr) {
+    const int r = t * 128 + warp * 16 + rr;
+    raw[rr] = r < N ? *reinterpret_cast<const uint2*>(src + static_cast<size_t>(r) * D + 4 * lane)
+                    : make_uint2(0u, 0u);
+  }
+  float m[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int c = 0; c < kVSlab; ++c)
-      m[c] = fmaxf(m[c], fabsf(to_f32<BF16>(static_cast<uint16_t>(w[c / 2] >> (16 * (c & 1))))));
+  for (int rr = 0; rr < 16; ++rr) {
+    m[0] = fmaxf(m[0], fabsf(to_f32<BF16>(static_cast<uint16_t>(raw[rr].x & 0xFFFFu))));
+    m[1] = fmaxf(m[1], fabsf(to_f32<BF16>(static_cast<uint16_t>(raw[rr].x >> 16))));
+    m[2] = fmaxf(m[2], fabsf(to_f32<BF16>(static_cast<uint16_t>(raw[rr].y & 0xFFFFu))));
+    m[3] = fmaxf(m[3], fabsf(to_f32<BF16>(static_cast<uint16_t>(raw[rr].y >> 16))));
   }
 #pragma unroll
-  for (int c = 0; c < kVSlab; ++c) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) m[c] = fmaxf(m[c], __shfl_xor_sync(0xffffffffu, m[c], off));
-    if (lane == 0) s_max[warp][c] = m[c];
-  }
+  for (int e = 0; e < 4; ++e) s_max[warp][4 * lane + e] = m[e];
   __syncthreads();
-  if (threadIdx.x < kVSlab) {
+  if (threadIdx.x < D) {
     float a = s_max[0][threadIdx.x];
 #pragma unroll
     for (int w = 1; w < kVThreads / 32; ++w) a = fmaxf(a, s_max[w][threadIdx.x]);
-    s_f[threadIdx.x] = a > 0.f ? 448.0f / a : 0.f;
-    v_scale[static_cast<size_t>(head) * D + c0 + threadIdx.x] = a * cfac;
+    atomicMax(v_amax_bits + static_cast<size_t>(head) * D + threadIdx.x, __float_as_uint(a));
+  }
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(kVThreads)
+    fa_fp8_v_encode_kernel(const uint16_t* __restrict__ v, const float* __restrict__ v_amax,
+                           uint8_t* __restrict__ v8t, int N, int Np, int T) {
+  constexpr int D = 128;
+  // Codes of the block, channel-major: row c holds keys t*128 .. t*128 + 127
+  // (+4 bytes of padding per row against bank conflicts on the transposed writes).
+  __shared__ uint32_t s_codes[D][128 / 4 + 1];
+  const int head = blockIdx.x / T;
+  const int t = blockIdx.x % T;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint16_t* src = v + static_cast<size_t>(head) * N * D;
+  float f[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float a = v_amax[static_cast<size_t>(head) * D + 4 * lane + e];
+    f[e] = a > 0.f ? 448.0f / a : 0.f;
+  }
+  // warp w encodes rows 16w .. 16w + 15 (channels 4 lane .. 4 lane + 3 per lane);
+  // four consecutive rows' codes of one channel form one 32-bit word
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t word[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const int rl = warp * 16 + q * 4 + b;  // row within the block
+      const int r = t * 128 + rl;
+      uint2 w = make_uint2(0u, 0u);
+      if (r < N) w = *reinterpret_cast<const uint2*>(src + static_cast<size_t>(r) * D + 4 * lane);
+      const float x[4] = {to_f32<BF16>(static_cast<uint16_t>(w.x & 0xFFFFu)),
+                          to_f32<BF16>(static_cast<uint16_t>(w.x >> 16)),
+                          to_f32<BF16>(static_cast<uint16_t>(w.y & 0xFFFFu)),
+                          to_f32<BF16>(static_cast<uint16_t>(w.y >> 16))};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) word[e] |= (r < N ? e4m3(x[e] * f[e]) : 0u) << (8 * b);
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) s_codes[4 * lane + e][warp * 4 + q] = word[e];
   }
   __syncthreads();
-  float f[kVSlab];
-#pragma unroll
-  for (int c = 0; c < kVSlab; ++c) f[c] = s_f[c];
-  uint8_t* dst = v8t + (static_cast<size_t>(head) * D + c0) * Np;
-  for (int r = threadIdx.x; r < Np; r += kVThreads) {
-    uint32_t w[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    if (r < N) {
-      const uint4* p = reinterpret_cast<const uint4*>(src + static_cast<size_t>(r) * D);
-      const uint4 w0 = p[0], w1 = p[1];
-      w[0] = w0.x; w[1] = w0.y; w[2] = w0.z; w[3] = w0.w;
-      w[4] = w1.x; w[5] = w1.y; w[6] = w1.z; w[7] = w1.w;
-    }
-#pragma unroll
-    for (int c = 0; c < kVSlab; ++c) {
-      const float x = to_f32<BF16>(static_cast<uint16_t>(w[c / 2] >> (16 * (c & 1))));
-      dst[static_cast<size_t>(c) * Np + r] = static_cast<uint8_t>(r < N ? e4m3(x * f[c]) : 0u);
-    }
+  // row c of the output gets keys t*128 .. t*128 + 127 of channel c, as 32 words
+  uint8_t* dst = v8t + static_cast<size_t>(head) * D * Np;
+  const int nbytes = (t * 128 + 128 <= Np) ? 128 : Np - t * 128;  // the last block may be short
+  for (int i = threadIdx.x; i < D * 32; i += kVThreads) {
+    const int c = i >> 5;
+    const int wi = i & 31;
+    if (4 * wi < nbytes)
+      *reinterpret_cast<uint32_t*>(dst + static_cast<size_t>(c) * Np + t * 128 + 4 * wi) = s_codes[c][wi];
   }
+}
+
+__global__ void fa_fp8_v_scale_kernel(float* __restrict__ v_scale, int n, float cfac) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) v_scale[i] = v_scale[i] * cfac;  // the slot holds amax until now
 }
 
 }  // namespace
@@ -209,13 +256,24 @@ cudaError_t launch_quantize_fp8(const AttnShape& s, const Fp8QuantArgs& a, cudaS
         a.q_scale, a.k_scale, qb, s.N, T, cfac_qk);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const int vb = s.B * s.Hkv * (128 / kVSlab);
+  const int heads_kv = s.B * s.Hkv;
+  const int nsc = heads_kv * 128;
+  if ((e = cudaMemsetAsync(a.v_scale, 0, sizeof(float) * nsc, stream)) != cudaSuccess) return e;
   if (s.bf16)
-    fa_fp8_v_kernel<true><<<vb, kVThreads, 0, stream>>>(static_cast<const uint16_t*>(a.v), a.v8t,
-                                                        a.v_scale, s.N, a.Np, cfac_v);
+    fa_fp8_v_amax_kernel<true><<<heads_kv * T, kVThreads, 0, stream>>>(
+        static_cast<const uint16_t*>(a.v), reinterpret_cast<unsigned int*>(a.v_scale), s.N, T);
   else
-    fa_fp8_v_kernel<false><<<vb, kVThreads, 0, stream>>>(static_cast<const uint16_t*>(a.v), a.v8t,
-                                                         a.v_scale, s.N, a.Np, cfac_v);
+    fa_fp8_v_amax_kernel<false><<<heads_kv * T, kVThreads, 0, stream>>>(
+        static_cast<const uint16_t*>(a.v), reinterpret_cast<unsigned int*>(a.v_scale), s.N, T);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (s.bf16)
+    fa_fp8_v_encode_kernel<true><<<heads_kv * T, kVThreads, 0, stream>>>(
+        static_cast<const uint16_t*>(a.v), a.v_scale, a.v8t, s.N, a.Np, T);
+  else
+    fa_fp8_v_encode_kernel<false><<<heads_kv * T, kVThreads, 0, stream>>>(
+        static_cast<const uint16_t*>(a.v), a.v_scale, a.v8t, s.N, a.Np, T);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  fa_fp8_v_scale_kernel<<<(nsc + 255) / 256, 256, 0, stream>>>(a.v_scale, nsc, cfac_v);
   return cudaGetLastError();
 }
 
