@@ -264,8 +264,14 @@ struct SplitPlan {
   int splits, chunk_tiles;
 };
 
-// Key chunks for the split-KV forward: enough CTAs for about two waves of the
-// device's SMs, at least one 128-key tile per chunk, no empty chunk.
+// Key chunks for the split-KV forward: at least one 128-key tile per chunk,
+// no empty chunk.  Chosen automatically, the split count s minimises the
+// modelled time waves(s) x (chunk(s) + 2): the CTAs (one per SM at a time)
+// run in ceil(base*s / SMs) waves, each as long as a chunk of ceil(KT / s)
+// key tiles plus a CTA's fixed cost (prologue and epilogue, about two tiles'
+// worth of loads).  A count that leaves a nearly empty last wave loses most
+// of a wave's time; this picks one that fills the waves (ties: fewer splits,
+// less merge work).  Chunks stay at least 4 tiles long.
 SplitPlan plan_splits(int B, int Hq, int Hkv, int Nq, int Nk, int requested) {
   const long Mq = static_cast<long>(Hq / Hkv) * Nq;
   const long base = ((Mq + 127) / 128) * B * Hkv;
@@ -275,7 +281,18 @@ SplitPlan plan_splits(int B, int Hq, int Hkv, int Nq, int Nk, int requested) {
     int sms = 148;
     int dev = 0;
     if (cudaGetDevice(&dev) == cudaSuccess) sms = fa::sm_count();
-    want = (2L * sms + base - 1) / base;
+    const long s_max = KT >= 8 ? KT / 4 : 1;
+    long best_cost = -1;
+    want = 1;
+    for (long sp = 1; sp <= s_max; ++sp) {
+      const long chunk = (KT + sp - 1) / sp;
+      const long waves = (base * sp + sms - 1) / sms;
+      const long cost = waves * (chunk + 2);
+      if (best_cost < 0 || cost < best_cost) {
+        best_cost = cost;
+        want = sp;
+      }
+    }
   }
   if (want < 1) want = 1;
   if (want > KT) want = KT;
