@@ -9,17 +9,23 @@
 // exponentiated against the running maximum and O is divided by l once at the
 // end, "Flash Attention", section "Online softmax").
 //
-// GB300 design (one CTA per pair of 128-row query tiles of one head):
-//   warp 8      TMA producer: Q tiles once, then K_j through a 3-stage and
-//               V_j through a 2-stage shared-memory ring (128-byte swizzle,
-//               3-D tensor maps over [B*H, N, d] so ragged tails are
-//               zero-filled).
+// GB300 design.  A work item is a pair of 128-row query tiles (A, B) of one
+// head; the grid has one CTA per item, and a running CTA takes over the items
+// of CTAs that have not started (cluster launch control), so each CTA runs
+// items back to back with its pipelines running on across item boundaries.
+//   warp 8      TMA producer and scheduler: claims and publishes the next item;
+//               Q tiles per item, then K_j through a 3-stage and V_j through a
+//               2-stage shared-memory ring (128-byte swizzle, 3-D tensor maps
+//               over [B*H, N, d] so ragged tails are zero-filled).
 //   warps 9-10  MMA issuers, one thread per query tile X: S_X = Q_X K_j^T into
 //               Tensor Memory, O_X += P_X V_j with P_X read from Tensor Memory
 //               (A operand) and V_j from shared memory as an MN-major B operand.
+//   warp 11     idle (completes the control warpgroup for register reallocation).
 //   warps 0-3   softmax for query tile A, warps 4-7 for tile B: thread t owns
 //               row t (TMEM lane t); exp2 with the scale folded in; P written
 //               back to TMEM as 16-bit pairs over the first half of S.
+// Instantiations: 16-bit (fp16/bf16), causal sliding window (WIN), and e4m3
+// inputs (F8) -- see the kernel's comment.
 // The two tiles ping-pong: while one softmax group works, the tensor core runs
 // the other tile's MMAs ("FlashAttention Primer", section "FlashAttention-3":
 // softmax of one block overlaps the matmuls of another; Figure 7).
