@@ -363,7 +363,10 @@ int fa_forward_splitkv(const void* q, const void* k, const void* v, void* o, flo
   return FA_OK;
 }
 
-int fa_fp8_vt_stride(int N) { return N <= 0 ? 0 : (N + 15) / 16 * 16; }
+int fa_fp8_vt_stride(int N) {
+  if (N <= 0 || N > 0x7fffffff - 15) return 0;
+  return (N + 15) / 16 * 16;
+}
 
 int fa_forward_fp8(const void* q8, const void* k8, const void* v8t, const float* q_scale,
                    const float* k_scale, const float* v_scale, void* o, float* lse, int B, int Hq,
@@ -404,6 +407,7 @@ int fa_quantize_fp8(const void* q, const void* k, const void* v, const signed ch
   int rc = check_common(B, Hq, Hkv, N, d, 1.0f, dtype);
   if (rc) return rc;
   if (d != 128) return fail(FA_ERR_UNSUPPORTED, "FP8 path: head dimension d=%d (supported: 128)", d);
+  if (fa_fp8_vt_stride(N) == 0) return fail(FA_ERR_UNSUPPORTED, "N=%d too large for the V code layout", N);
   const void* ptrs[] = {q, k, v, q8, k8, v8t, q_scale, k_scale, v_scale};
   for (const void* p : ptrs)
     if (!aligned16(p)) return fail(FA_ERR_UNSUPPORTED, "all tensor pointers must be 16-byte aligned");

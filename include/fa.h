@@ -132,7 +132,7 @@ FA_API int fa_forward_window(const void* q, const void* k, const void* v, void* 
  * Both allocate nothing, run asynchronously on `stream`, and return the
  * fa_forward error codes (FA_ERR_UNSUPPORTED for d != 128).
  */
-FA_API int fa_fp8_vt_stride(int N);
+FA_API int fa_fp8_vt_stride(int N);  /* Np for N >= 1 (0 if N < 1 or Np would overflow an int) */
 FA_API int fa_quantize_fp8(const void* q, const void* k, const void* v, const signed char* signs,
                            void* q8, void* k8, void* v8t, float* q_scale, float* k_scale,
                            float* v_scale, int B, int Hq, int Hkv, int N, int d, int dtype,

@@ -121,7 +121,7 @@ def test_fp8_entry_points_validate_before_device_work(lib):
     fake = ctypes.c_void_p(4096)
     null = ctypes.c_void_p(0)
     assert lib.fa_fp8_vt_stride(1) == 16 and lib.fa_fp8_vt_stride(300) == 304
-    assert lib.fa_fp8_vt_stride(0) == 0
+    assert lib.fa_fp8_vt_stride(0) == 0 and lib.fa_fp8_vt_stride(2 ** 31 - 1) == 0
     # d must be 128
     assert lib.fa_quantize_fp8(fake, fake, fake, null, fake, fake, fake, fake, fake, fake,
                                1, 1, 1, 8, 64, 1, null) == 2
