@@ -128,10 +128,12 @@ __device__ __forceinline__ int window_first_tile(int t, int window) {
   return first_key > 0 ? first_key / kBN : 0;
 }
 
+// per: query tiles per item, 2 (tiles 2p and 2p + 1) or 1 (tile p alone, no
+// tile B), the latter when pairs would leave SMs idle.
 template <bool WIN>
 __device__ __forceinline__ FwdItem decode_item(int item, int heads, int head_group, int Hq,
-                                               int Hkv, int T, int causal, int window) {
-  const int pairs = (T + 1) / 2;
+                                               int Hkv, int T, int causal, int window, int per) {
+  const int pairs = (T + per - 1) / per;
   // Groups of heads whose K and V stay in L2; heaviest causal pairs first.
   const WorkItem wi = grouped_heavy_first(item, heads, pairs, head_group);
   const int pair = pairs - 1 - wi.rank;
@@ -140,8 +142,8 @@ __device__ __forceinline__ FwdItem decode_item(int item, int heads, int head_gro
   const int h = it.bh % Hq;
   const int b = it.bh / Hq;
   it.kvh = b * Hkv + h / (Hq / Hkv);
-  it.tA = 2 * pair;
-  it.tB = 2 * pair + 1;
+  it.tA = per * pair;
+  it.tB = per == 2 ? per * pair + 1 : T;
   const bool hasB = it.tB < T;
   it.loA = WIN ? window_first_tile(it.tA, window) : 0;
   it.loB = (WIN && hasB) ? window_first_tile(it.tB, window) : it.loA;
@@ -173,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, void* __restrict__ out,
                   float* __restrict__ lse_out, int heads, int head_group, int Hq, int Hkv, int N,
-                  int causal, int window, float scale_log2, const float* __restrict__ q_scale,
+                  int causal, int window, int per, float scale_log2, const float* __restrict__ q_scale,
                   const float* __restrict__ k_scale, const float* __restrict__ v_scale, int* err) {
   static_assert(!F8 || (D == 128 && BF16 && !WIN), "e4m3 path: d = 128, bfloat16 output, no window");
   constexpr int kElt = F8 ? 1 : 2;
@@ -249,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         item_slot[slot] = item;
         mbar_arrive(&bar[BITEMFULL + slot]);  // release: the slot write is visible to waiters
         if (item < 0) break;
-        const FwdItem it = decode_item<WIN>(item, heads, head_group, Hq, Hkv, T, causal, window);
+        const FwdItem it = decode_item<WIN>(item, heads, head_group, Hq, Hkv, T, causal, window, per);
         // Query tiles: buffer X is free once the previous item's last S_X has completed.
         for (int X = 0; X < 2 && ok; ++X) {
           const int nX = X ? it.nB : it.nA;
@@ -383,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&bar[BITEMEMPTY + (count & 1)]);
       if (item < 0) break;
       if (lane == 0) {
-        const FwdItem it = decode_item<WIN>(item, heads, head_group, Hq, Hkv, T, causal, window);
+        const FwdItem it = decode_item<WIN>(item, heads, head_group, Hq, Hkv, T, causal, window, per);
         const int nX = X ? it.nB : it.nA;
         // Key tiles of the item's stream this query tile does not visit (under
         // a sliding window, tile B skips the first one; under causal masking
@@ -469,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar[BITEMEMPTY + (count & 1)]);
       if (item < 0) break;
-      const FwdItem it = decode_item<WIN>(item, heads, head_group, Hq, Hkv, T, causal, window);
+      const FwdItem it = decode_item<WIN>(item, heads, head_group, Hq, Hkv, T, causal, window, per);
       const int t = X ? it.tB : it.tA;
       const int nX = X ? it.nB : it.nA;
       const int loX = X ? it.loB : it.loA;  // key tile of round 0
@@ -690,8 +692,10 @@ cudaError_t launch_fwd_t(const AttnShape& s, const FwdArgs& a, cudaStream_t stre
                                 F8 ? 28 : (WIN ? 4 : 0) + (D == 64 ? 0 : 2) + (BF16 ? 1 : 0));
   if (e != cudaSuccess) return e;
   const int T = (s.N + kBM - 1) / kBM;
-  const int pairs = (T + 1) / 2;
-  dim3 grid(static_cast<unsigned>(pairs * s.B * s.Hq));  // (head, pair) work items
+  // Work items of two query tiles, or of one when pairs would not fill the SMs.
+  const int per = (static_cast<long>((T + 1) / 2) * s.B * s.Hq < sm_count()) ? 1 : 2;
+  const int items_per_head = (T + per - 1) / per;
+  dim3 grid(static_cast<unsigned>(items_per_head * s.B * s.Hq));  // (head, item) work items
   const float scale_log2 = s.scale * 1.4426950408889634f;
   // Heads side by side so that their K and V (4*N*d bytes per KV head, shared
   // by Hq/Hkv query heads) stay within about a quarter of the L2.
@@ -700,7 +704,7 @@ cudaError_t launch_fwd_t(const AttnShape& s, const FwdArgs& a, cudaStream_t stre
   hg = hg < 1 ? 1 : (hg > 64 ? 64 : hg);
   kern<<<grid, kThreads, smem, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.o, a.lse, s.B * s.Hq,
                                          static_cast<int>(hg), s.Hq, s.Hkv, s.N, s.causal,
-                                         s.window, scale_log2, a.q_scale, a.k_scale, a.v_scale,
+                                         s.window, per, scale_log2, a.q_scale, a.k_scale, a.v_scale,
                                          a.err);
   return cudaGetLastError();
 }
