@@ -352,37 +352,75 @@ def run_ours(args):
     f_fwd, f_bwd = flops_per_step()
     value = whole_job_tflops(f_fwd + f_bwd, K, world, elapsed_ms)
 
-    # end-to-end through the public API with pinned host buffers: H2D of the
-    # step's inputs, forward, backward, D2H of the gradients, every step.
+    # End to end through the public API with pinned host buffers: every step
+    # copies its inputs in (H2D), runs forward + backward, and reads its
+    # gradients back (D2H).  Steps are pipelined the way a training loop
+    # feeds an accelerator: step i+1's inputs travel on a copy stream and
+    # step i-1's gradients on another while step i computes, with device
+    # inputs and outputs double-buffered and every dependency an event.  The
+    # timed region runs from before the first step's H2D to after the last
+    # step's D2H, so every step's copies are inside it.
     host = {n: inp[n].pin_memory() for n in ("q", "k", "v", "dO")}
     out_h = {n: torch.empty(t.shape, dtype=t.dtype).pin_memory() for n, t in (("dq", dq), ("dk", dk), ("dv", dv))}
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = sum(t.numel() * t.element_size() for t in out_h.values())
     E = max(3, min(K, 20))
+    dev_in = [{"q": q, "k": k, "v": v, "dO": dO},
+              {n: torch.empty_like(t) for n, t in (("q", q), ("k", k), ("v", v), ("dO", dO))}]
+    dev_out = [{"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv},
+               {"o": torch.empty_like(o), "lse": torch.empty_like(lse), "dq": torch.empty_like(dq),
+                "dk": torch.empty_like(dk), "dv": torch.empty_like(dv)}]
+    s_h2d, s_d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
 
-    def e2e_step():
-        q.copy_(host["q"], non_blocking=True)
-        k.copy_(host["k"], non_blocking=True)
-        v.copy_(host["v"], non_blocking=True)
-        dO.copy_(host["dO"], non_blocking=True)
-        step()
-        out_h["dq"].copy_(dq, non_blocking=True)
-        out_h["dk"].copy_(dk, non_blocking=True)
-        out_h["dv"].copy_(dv, non_blocking=True)
+    def e2e_run(n_steps, e_start=None, e_end=None):
+        comp_done = [None, None]  # compute of the last step that used buffer set b
+        d2h_done = [None, None]   # read-back of the last step that used buffer set b
+        if e_start is not None:
+            e_start.record(stream)
+            s_h2d.wait_stream(stream)
+        last = None
+        for i in range(n_steps):
+            bset = i % 2
+            di, do_ = dev_in[bset], dev_out[bset]
+            with torch.cuda.stream(s_h2d):
+                if comp_done[bset] is not None:
+                    s_h2d.wait_event(comp_done[bset])  # step i-2 is done reading these inputs
+                for n_ in ("q", "k", "v", "dO"):
+                    di[n_].copy_(host[n_], non_blocking=True)
+                h2d_ev = torch.cuda.Event()
+                h2d_ev.record(s_h2d)
+            stream.wait_event(h2d_ev)
+            if d2h_done[bset] is not None:
+                stream.wait_event(d2h_done[bset])  # step i-2's gradients have been read back
+            forward(di["q"], di["k"], di["v"], causal=True, scale=scale, out=do_["o"], lse=do_["lse"],
+                    stream=stream)
+            backward(di["q"], di["k"], di["v"], do_["o"], do_["lse"], di["dO"], causal=True, scale=scale,
+                     dq=do_["dq"], dk=do_["dk"], dv=do_["dv"], workspace=ws, stream=stream)
+            comp_done[bset] = torch.cuda.Event()
+            comp_done[bset].record(stream)
+            with torch.cuda.stream(s_d2h):
+                s_d2h.wait_event(comp_done[bset])
+                for n_ in ("dq", "dk", "dv"):
+                    out_h[n_].copy_(do_[n_], non_blocking=True)
+                d2h_done[bset] = torch.cuda.Event()
+                d2h_done[bset].record(s_d2h)
+            last = d2h_done[bset]
+        stream.wait_event(last)
+        if e_end is not None:
+            e_end.record(stream)
 
-    e2e_step()
+    e2e_run(2)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(E):
-        e2e_step()
-    e1.record(stream)
+    e2e_run(E, e0, e1)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     check_errors()
     e2e_value = whole_job_tflops(f_fwd + f_bwd, E, world, e2e_ms)
+    # the last step's gradients, read back through the pipeline, equal the device result
+    e2e_check = bool(torch.equal(out_h["dq"], dev_out[(E - 1) % 2]["dq"].cpu()))
 
     if rank == 0:
         peaks, peak_kind = load_peaks()
@@ -439,7 +477,11 @@ def run_ours(args):
             },
             "clocks": clocks,
             "e2e": {"value": e2e_value, "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "steps": E},
+                    "d2h_bytes_per_step": d2h, "steps": E, "ms_per_step": e2e_ms / E,
+                    "pipelined": "H2D of step i+1 and D2H of step i-1 overlap step i's compute "
+                                 "(separate copy streams, double-buffered device tensors); the "
+                                 "host copies (940 MB per step at ~0.3 TB/s) bound it",
+                    "readback_matches_device": e2e_check},
             "gpu_launches": 3 * K,
         }
         if not args.skip_workloads:
