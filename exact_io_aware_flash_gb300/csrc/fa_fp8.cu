@@ -41,8 +41,10 @@ __device__ __forceinline__ uint32_t e4m3(float x) {
   return static_cast<uint32_t>(__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3));
 }
 
-// Q and K, d = 128.  One CTA (8 warps) per (tensor, head, 128-row block); warp w
-// owns rows 16w .. 16w + 15 of the block, lane l channels 4l .. 4l + 3.
+// Q and K, d = 128.  One CTA (8 warps) per (tensor, head, 128-row block).  A
+// row belongs to 4 lanes, lane 4r + s holding channels 32s .. 32s + 31 of row r
+// of its group of 8; warp w handles rows 16w .. 16w + 15 in two groups of 8.
+// Butterfly stages 1 .. 16 run inside a lane, stages 32 and 64 across lanes.
 constexpr int kQkThreads = 256;
 
 template <bool BF16>
@@ -55,63 +57,67 @@ __global__ void __launch_bounds__(kQkThreads)
   __shared__ float s_max[kQkThreads / 32];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int sub = lane & 3;   // channels 32*sub .. 32*sub + 31
+  const int rsub = lane >> 2; // row within a group of 8
   const bool is_q = static_cast<int>(blockIdx.x) < q_blocks;
   const int blk = is_q ? blockIdx.x : blockIdx.x - q_blocks;  // head * T + block
   const int head = blk / T;
   const int t = blk % T;
   const uint16_t* src = (is_q ? q : k) + static_cast<size_t>(head) * N * D;
   uint8_t* dst = (is_q ? q8 : k8) + static_cast<size_t>(head) * N * D;
-  bool neg[4] = {false, false, false, false};
-  if (signs) {
+  // Both groups' loads are issued before any butterfly (the kernel is bound by
+  // memory latency, not arithmetic).
+  uint4 raw[2][4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) neg[e] = signs[4 * lane + e] < 0;
-  }
-  // All 16 rows' loads are issued before any butterfly, so that they are in
-  // flight together (the kernel is bound by memory latency, not arithmetic).
-  uint2 raw[16];
+  for (int g = 0; g < 2; ++g) {
+    const int r = t * 128 + warp * 16 + g * 8 + rsub;
 #pragma unroll
-  for (int rr = 0; rr < 16; ++rr) {
-    const int r = t * 128 + warp * 16 + rr;
-    raw[rr] = r < N ? *reinterpret_cast<const uint2*>(src + static_cast<size_t>(r) * D + 4 * lane)
-                    : make_uint2(0u, 0u);
+    for (int c = 0; c < 4; ++c)
+      raw[g][c] = r < N ? *reinterpret_cast<const uint4*>(src + static_cast<size_t>(r) * D + 32 * sub + 8 * c)
+                        : make_uint4(0u, 0u, 0u, 0u);
   }
-  float y[16][4];
+  float y[2][32];
   float amax = 0.f;
 #pragma unroll
-  for (int rr = 0; rr < 16; ++rr) {
-    const uint2 w = raw[rr];
-    float a[4];
-    a[0] = to_f32<BF16>(static_cast<uint16_t>(w.x & 0xFFFFu));
-    a[1] = to_f32<BF16>(static_cast<uint16_t>(w.x >> 16));
-    a[2] = to_f32<BF16>(static_cast<uint16_t>(w.y & 0xFFFFu));
-    a[3] = to_f32<BF16>(static_cast<uint16_t>(w.y >> 16));
+  for (int g = 0; g < 2; ++g) {
+    float* a = y[g];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint32_t w[4] = {raw[g][c].x, raw[g][c].y, raw[g][c].z, raw[g][c].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        a[8 * c + 2 * e] = to_f32<BF16>(static_cast<uint16_t>(w[e] & 0xFFFFu));
+        a[8 * c + 2 * e + 1] = to_f32<BF16>(static_cast<uint16_t>(w[e] >> 16));
+      }
+    }
     if (signs) {
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        if (neg[e]) a[e] = -a[e];
+      for (int e = 0; e < 32; ++e)
+        if (signs[32 * sub + e] < 0) a[e] = -a[e];
       // Butterfly stage h pairs channel i (bit h clear) with i + h: (a + b, a - b).
-      // h = 1, 2: inside the lane's four channels.
-      float b0 = a[0] + a[1], b1 = a[0] - a[1], b2 = a[2] + a[3], b3 = a[2] - a[3];
-      a[0] = b0 + b2;
-      a[2] = b0 - b2;
-      a[1] = b1 + b3;
-      a[3] = b1 - b3;
-      // h = 4 .. 64: channel 4l + e pairs with 4(l ^ m) + e, m = h / 4.
 #pragma unroll
-      for (int m = 1; m < 32; m <<= 1) {
-        const bool lower = (lane & m) == 0;
+      for (int h = 1; h < 32; h <<= 1) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
+        for (int e = 0; e < 32; ++e)
+          if ((e & h) == 0) {
+            const float lo = a[e], hi = a[e + h];
+            a[e] = lo + hi;
+            a[e + h] = lo - hi;
+          }
+      }
+      // h = 32, 64: channel 32s + e pairs with 32(s ^ m) + e, m = h / 32.
+#pragma unroll
+      for (int m = 1; m < 4; m <<= 1) {
+        const bool lower = (sub & m) == 0;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
           const float other = __shfl_xor_sync(0xffffffffu, a[e], m);
           a[e] = lower ? a[e] + other : other - a[e];
         }
       }
     }
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      y[rr][e] = a[e];
-      amax = fmaxf(amax, fabsf(a[e]));
-    }
+    for (int e = 0; e < 32; ++e) amax = fmaxf(amax, fabsf(a[e]));
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
@@ -123,12 +129,17 @@ __global__ void __launch_bounds__(kQkThreads)
   const float f = amax > 0.f ? 448.0f / amax : 0.f;
   if (threadIdx.x == 0) (is_q ? q_scale : k_scale)[blk] = amax * cfac;
 #pragma unroll
-  for (int rr = 0; rr < 16; ++rr) {
-    const int r = t * 128 + warp * 16 + rr;
+  for (int g = 0; g < 2; ++g) {
+    const int r = t * 128 + warp * 16 + g * 8 + rsub;
     if (r < N) {
-      const uint32_t c = e4m3(y[rr][0] * f) | (e4m3(y[rr][1] * f) << 8) | (e4m3(y[rr][2] * f) << 16) |
-                         (e4m3(y[rr][3] * f) << 24);
-      *reinterpret_cast<uint32_t*>(dst + static_cast<size_t>(r) * D + 4 * lane) = c;
+      uint32_t c[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        c[e] = e4m3(y[g][4 * e] * f) | (e4m3(y[g][4 * e + 1] * f) << 8) |
+               (e4m3(y[g][4 * e + 2] * f) << 16) | (e4m3(y[g][4 * e + 3] * f) << 24);
+      uint4* o = reinterpret_cast<uint4*>(dst + static_cast<size_t>(r) * D + 32 * sub);
+      o[0] = make_uint4(c[0], c[1], c[2], c[3]);
+      o[1] = make_uint4(c[4], c[5], c[6], c[7]);
     }
   }
 }
