@@ -623,6 +623,8 @@ def workload_table(dev, peaks):
     out["backward_sweep"] = bwd
     # FP8 (e4m3) forward on the two large forward workloads' shapes: quantization
     # (rotation + block scales, HBM-bound) and attention over the codes
+    import numpy as np
+
     from exact_io_aware_flash_gb300 import forward_fp8, quantize_fp8
     fp8_peak = 2.0 * burst  # e4m3 dense rate = 2x the 16-bit rate (nominal ratio)
     fp8 = {"peak_tflops": fp8_peak,
@@ -631,8 +633,7 @@ def workload_table(dev, peaks):
         s_ = WORKLOADS[name]["shape"]
         inp = make_inputs(s_, "bf16", seed=WORKLOADS[name]["seed"], with_dO=False)
         q, k, v = (inp[n].to(dev) for n in ("q", "k", "v"))
-        signs = torch.from_numpy(
-            __import__("numpy").random.default_rng(0).choice([-1, 1], s_.d).astype("int8")).to(dev)
+        signs = torch.from_numpy(np.random.default_rng(0).choice([-1, 1], s_.d).astype(np.int8)).to(dev)
         codes = quantize_fp8(q, k, v, signs)
         o = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
         lse = torch.empty(s_.B, s_.Hq, s_.N, dtype=torch.float32, device=dev)

@@ -482,14 +482,14 @@ int oracle_fp8_quantize_qk(const float* x, const signed char* signs, int heads, 
     int failed = 0;
 #pragma omp parallel
     {
-    float* y = (float*)malloc(sizeof(float) * (size_t)128 * d);
-    if (!y) {
+        float* y = (float*)malloc(sizeof(float) * (size_t)128 * d);
+        if (!y) {
 #pragma omp atomic write
-        failed = 1;
-    }
-    /* blocks are independent: the same result for any thread count */
+            failed = 1;
+        }
+        /* blocks are independent: the same result for any thread count */
 #pragma omp for schedule(dynamic, 1)
-    for (long ht = 0; ht < (long)heads * T; ++ht) {
+        for (long ht = 0; ht < (long)heads * T; ++ht) {
             if (!y) continue;
             const int h = (int)(ht / T), t = (int)(ht % T);
             const int r0 = t * 128, r1 = (r0 + 128 < N) ? r0 + 128 : N;
@@ -508,8 +508,8 @@ int oracle_fp8_quantize_qk(const float* x, const signed char* signs, int heads, 
                 for (int c = 0; c < d; ++c)
                     codes[((size_t)h * N + r) * d + c] =
                         (unsigned char)oracle_e4m3_encode(y[(size_t)(r - r0) * d + c] * f);
-    }
-    free(y);
+        }
+        free(y);
     }
     return failed ? ORACLE_ENOMEM : ORACLE_OK;
 }
@@ -525,18 +525,18 @@ int oracle_fp8_quantize_v(const float* v, int heads, int N, int d, unsigned char
     /* (head, channel) pairs are independent: the same result for any thread count */
 #pragma omp parallel for schedule(dynamic, 1)
     for (long hc = 0; hc < (long)heads * d; ++hc) {
-            const int h = (int)(hc / d), c = (int)(hc % d);
-            float amax = 0.f;
-            for (int r = 0; r < N; ++r) {
-                const float a = fabsf(v[((size_t)h * N + r) * d + c]);
-                if (a > amax) amax = a;
-            }
-            const float f = amax > 0.f ? 448.0f / amax : 0.f;
-            scales[(size_t)h * d + c] = amax * cfac;
-            for (int r = 0; r < N; ++r) {
-                const size_t e = ((size_t)h * N + r) * d + c;
-                codes[e] = (unsigned char)oracle_e4m3_encode(v[e] * f);
-            }
+        const int h = (int)(hc / d), c = (int)(hc % d);
+        float amax = 0.f;
+        for (int r = 0; r < N; ++r) {
+            const float a = fabsf(v[((size_t)h * N + r) * d + c]);
+            if (a > amax) amax = a;
+        }
+        const float f = amax > 0.f ? 448.0f / amax : 0.f;
+        scales[(size_t)h * d + c] = amax * cfac;
+        for (int r = 0; r < N; ++r) {
+            const size_t e = ((size_t)h * N + r) * d + c;
+            codes[e] = (unsigned char)oracle_e4m3_encode(v[e] * f);
+        }
     }
     return ORACLE_OK;
 }
