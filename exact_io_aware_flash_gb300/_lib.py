@@ -54,6 +54,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.fa_backward.restype = i
         lib.fa_backward_window.argtypes = [vp] * 10 + [sz] + [i] * 6 + [f, i, vp]
         lib.fa_backward_window.restype = i
+        lib.fa_backward_atomic_workspace_size.argtypes = [i, i, i, i]
+        lib.fa_backward_atomic_workspace_size.restype = sz
+        lib.fa_backward_atomic.argtypes = [vp] * 10 + [sz] + [i] * 7 + [f, i, vp]
+        lib.fa_backward_atomic.restype = i
         lib.fa_fp8_vt_stride.argtypes = [i]
         lib.fa_fp8_vt_stride.restype = i
         lib.fa_quantize_fp8.argtypes = [vp] * 10 + [i] * 6 + [vp]
@@ -114,8 +118,12 @@ def version() -> str:
     return load().fa_version().decode()
 
 
-def workspace_size(B: int, Hq: int, N: int, d: int) -> int:
-    return int(load().fa_backward_workspace_size(B, Hq, N, d))
+def workspace_size(B: int, Hq: int, N: int, d: int, deterministic: bool = True) -> int:
+    """Bytes of backward workspace (fa_backward, or fa_backward_atomic when not deterministic)."""
+    lib = load()
+    if deterministic:
+        return int(lib.fa_backward_workspace_size(B, Hq, N, d))
+    return int(lib.fa_backward_atomic_workspace_size(B, Hq, N, d))
 
 
 def _window_arg(window, causal) -> int:
@@ -258,10 +266,14 @@ def forward_splitkv(q, k, v, scale: float | None = None, num_splits: int = 0, ou
 
 
 def backward(q, k, v, o, lse, dO, causal: bool = False, scale: float | None = None, dq=None,
-             dk=None, dv=None, workspace=None, stream=None, window: int | None = None):
+             dk=None, dv=None, workspace=None, stream=None, window: int | None = None,
+             deterministic: bool = True):
     """dq, dk, dv of O = softmax(scale q k^T) v given the forward's o, lse and dO = dL/dO.
 
-    window: the forward's sliding window (with causal=True), through fa_backward_window.
+    window: the forward's sliding window (with causal=True).
+    deterministic: True runs fa_backward / fa_backward_window (two passes, every
+    sum in a fixed order); False runs fa_backward_atomic (one pass, dq summed
+    with atomic adds, so its last bits vary between runs).
     """
     B, Hq, N, d = q.shape
     Hkv = k.shape[1]
@@ -276,7 +288,7 @@ def backward(q, k, v, o, lse, dO, causal: bool = False, scale: float | None = No
     _check(dq, "dq", (B, Hq, N, d), q.dtype)
     _check(dk, "dk", (B, Hkv, N, d), q.dtype)
     _check(dv, "dv", (B, Hkv, N, d), q.dtype)
-    ws_bytes = workspace_size(B, Hq, N, d)
+    ws_bytes = workspace_size(B, Hq, N, d, deterministic)
     if workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
     if workspace.numel() * workspace.element_size() < ws_bytes:
@@ -285,7 +297,11 @@ def backward(q, k, v, o, lse, dO, causal: bool = False, scale: float | None = No
     ptrs = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dO.data_ptr(),
             dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(),
             workspace.numel() * workspace.element_size())
-    if window is not None:
+    if not deterministic:
+        w = 0 if window is None else _window_arg(window, causal)
+        rc = lib.fa_backward_atomic(*ptrs, B, Hq, Hkv, N, d, int(bool(causal)), w, float(scale),
+                                    _dtype_code(q), _stream_handle(stream))
+    elif window is not None:
         rc = lib.fa_backward_window(*ptrs, B, Hq, Hkv, N, d, _window_arg(window, causal),
                                     float(scale), _dtype_code(q), _stream_handle(stream))
     else:

@@ -179,11 +179,11 @@ int sm_count() {
 
 cudaError_t set_smem_once(const void* kernel, int bytes, int slot) {
   // slot: a small per-kernel index; one flag per (device, slot)
-  static std::atomic<int> done[kMaxDevices][32];
+  static std::atomic<int> done[kMaxDevices][64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices || slot < 0 || slot >= 32)
+  if (dev < 0 || dev >= kMaxDevices || slot < 0 || slot >= 64)
     return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (done[dev][slot].load(std::memory_order_acquire)) return cudaSuccess;
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
@@ -437,20 +437,28 @@ size_t fa_backward_workspace_size(int B, int Hq, int N, int d) {
   return round_up(rows * 4, 256);
 }
 
+size_t fa_backward_atomic_workspace_size(int B, int Hq, int N, int d) {
+  if (B <= 0 || Hq <= 0 || N <= 0 || d <= 0) return 0;
+  const size_t rows = static_cast<size_t>(B) * Hq * N;
+  return round_up(rows * 4, 256) + round_up(rows * static_cast<size_t>(d) * 4, 256);
+}
+
 }  // extern "C"
 
 namespace {
 
-// Shared body of fa_backward and fa_backward_window (window as in forward_impl).
+// Shared body of fa_backward, fa_backward_window (window as in forward_impl)
+// and, with atomic = true, fa_backward_atomic.
 int backward_impl(const void* q, const void* k, const void* v, const void* o, const float* lse,
                   const void* dO, void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
                   int B, int Hq, int Hkv, int N, int d, int causal, int window, float scale,
-                  int dtype, void* stream) {
+                  int dtype, void* stream, bool atomic = false) {
   if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv || !workspace)
     return fail(FA_ERR_INVALID, "null tensor pointer");
   int rc = check_common(B, Hq, Hkv, N, d, scale, dtype);
   if (rc) return rc;
-  const size_t need = fa_backward_workspace_size(B, Hq, N, d);
+  const size_t need = atomic ? fa_backward_atomic_workspace_size(B, Hq, N, d)
+                             : fa_backward_workspace_size(B, Hq, N, d);
   if (ws_bytes < need)
     return fail(FA_ERR_INVALID, "workspace of %zu bytes is smaller than the %zu required", ws_bytes, need);
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
@@ -466,8 +474,10 @@ int backward_impl(const void* q, const void* k, const void* v, const void* o, co
   if ((rc = encode_tile_map(&a.tm_k, k, B * Hkv, N, d, s.bf16, "k"))) return rc;
   if ((rc = encode_tile_map(&a.tm_v, v, B * Hkv, N, d, s.bf16, "v"))) return rc;
   if ((rc = encode_tile_map(&a.tm_do, dO, B * Hq, N, d, s.bf16, "dO"))) return rc;
-  if ((rc = encode_tile_map(&a.tm_o, o, B * Hq, N, d, s.bf16, "o"))) return rc;
-  if ((rc = encode_tile_map(&a.tm_dq, dq, B * Hq, N, d, s.bf16, "dq", 32))) return rc;
+  if (!atomic) {  // the one-pass kernels read O and write dq with plain vector accesses
+    if ((rc = encode_tile_map(&a.tm_o, o, B * Hq, N, d, s.bf16, "o"))) return rc;
+    if ((rc = encode_tile_map(&a.tm_dq, dq, B * Hq, N, d, s.bf16, "dq", 32))) return rc;
+  }
   if ((rc = encode_tile_map(&a.tm_dk, dk, B * Hkv, N, d, s.bf16, "dk", 32))) return rc;
   if ((rc = encode_tile_map(&a.tm_dv, dv, B * Hkv, N, d, s.bf16, "dv", 32))) return rc;
   a.o = o;
@@ -481,7 +491,14 @@ int backward_impl(const void* q, const void* k, const void* v, const void* o, co
   a.ev_before_dq = t_ev_hooks[0];
   a.ev_before_dkdv = t_ev_hooks[1];
   a.ev_after_dkdv = t_ev_hooks[2];
-  cudaError_t e = fa::launch_backward(s, a, static_cast<cudaStream_t>(stream));
+  cudaError_t e;
+  if (atomic) {
+    float* dq_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                             fa_backward_workspace_size(B, Hq, N, d));
+    e = fa::launch_backward_atomic(s, a, dq_acc, static_cast<cudaStream_t>(stream));
+  } else {
+    e = fa::launch_backward(s, a, static_cast<cudaStream_t>(stream));
+  }
   if (e != cudaSuccess) return fail(FA_ERR_CUDA, "backward launch: %s", cudaGetErrorString(e));
   return FA_OK;
 }
@@ -507,6 +524,17 @@ int fa_backward_window(const void* q, const void* k, const void* v, const void* 
   if (window < 1) return fail(FA_ERR_INVALID, "window must be at least 1 (got %d)", window);
   return backward_impl(q, k, v, o, lse, dO, dq, dk, dv, workspace, ws_bytes, B, Hq, Hkv, N, d, 1,
                        window < N ? window : 0, scale, dtype, stream);
+}
+
+int fa_backward_atomic(const void* q, const void* k, const void* v, const void* o,
+                       const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                       void* workspace, size_t ws_bytes, int B, int Hq, int Hkv, int N, int d,
+                       int causal, int window, float scale, int dtype, void* stream) {
+  t_last_error.clear();
+  if (window < 0) return fail(FA_ERR_INVALID, "window must be 0 (none) or at least 1 (got %d)", window);
+  if (window > 0 && !causal) return fail(FA_ERR_INVALID, "a sliding window needs causal = 1");
+  return backward_impl(q, k, v, o, lse, dO, dq, dk, dv, workspace, ws_bytes, B, Hq, Hkv, N, d,
+                       causal, window < N ? window : 0, scale, dtype, stream, true);
 }
 
 int fa_set_backward_event_hooks(void* before_dq, void* before_dkdv, void* after_dkdv) {

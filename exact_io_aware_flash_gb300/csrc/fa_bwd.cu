@@ -27,6 +27,8 @@
 //                          S^T  = K_j Q_i^T,  dP^T = V_j dO_i^T   (SMEM x SMEM)
 //                          P^T, dS^T                           (compute warps)
 //                          dV  += P^T dO_i,   dK  += dS^T Q_i     (TMEM A operand)
+//                        Its body (dkdv_body.cuh) is shared with the one-pass
+//                        backward of fa_bwd_atomic.cu.
 // Outputs leave as 16-bit tiles staged in idle shared memory and written by
 // TMA stores (a thread-per-row global store pattern costs a whole iteration).
 // dQ is therefore summed over key tiles inside one CTA rather than with atomic
@@ -36,486 +38,31 @@
 // bitwise deterministic; the price is recomputing S and dP in both kernels
 // (7 instead of 5 N x N x d products).
 //
-// Both main kernels use 6 warps: warps 0-3 compute (thread t owns row t of the
+// Both kernels use 6 warps: warps 0-3 compute (thread t owns row t of the
 // tile, TMEM lane t), warp 4 is the TMA producer, warp 5 the single-thread MMA
 // issuer and TMEM allocator.
+#include "dkdv_body.cuh"
 #include "fa_internal.h"
-#include "ptx.cuh"
-
-#include <cuda_bf16.h>
-#include <cuda_fp16.h>
 
 namespace fa {
 namespace {
 
-constexpr int kBlk = 128;          // rows per tile (keys and queries)
-constexpr int kAtomBytes = 16384;  // 128 rows x 128 bytes
-constexpr int kThreads = 192;
-constexpr float kLog2e = 1.4426950408889634f;
+using namespace bwd;
 
-template <bool BF16>
-__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
-  if constexpr (BF16) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&v);
-  } else {
-    __half2 v = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&v);
-  }
-}
-
-template <bool BF16>
-__device__ __forceinline__ float2 unpack2(uint32_t w) {
-  if constexpr (BF16) {
-    __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&w);
-    return __bfloat1622float2(v);
-  } else {
-    __half2 v = *reinterpret_cast<__half2*>(&w);
-    return __half22float2(v);
-  }
-}
-
-__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
-  const unsigned long long t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer_ns() - t0 > 200000000ull) break;
-  }
-}
-
-__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
-  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) &
-                                    ~static_cast<uintptr_t>(1023));
-}
-
-// K-major operand (rows of 128 bytes, 8-row groups 1024 bytes apart), k-step ks of 16 elements.
-__device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile, int ks) {
-  return sdesc_sw128(tile + (ks >> 2) * kAtomBytes + (ks & 3) * 32, 16, 1024);
-}
-// MN-major operand over a [128 K-rows][D] tile, k-step ks of 16 K-rows.
-__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile, int ks) {
-  return sdesc_sw128(tile + ks * 2048, kAtomBytes, 1024);
-}
-// The same descriptors from the k-step-0 descriptor d0 of the tile: only the
-// start-address field (bits 0-13, address >> 4) moves, and shared-memory
-// addresses stay below 2^18, so one add of a compile-time constant per
-// operand replaces the full encoding in the MMA-issuing thread, whose
-// instruction count is on every iteration's critical path.
-__device__ __forceinline__ uint64_t kmajor_step(uint64_t d0, int ks) {
-  return d0 + static_cast<uint64_t>(((ks >> 2) * kAtomBytes + (ks & 3) * 32) >> 4);
-}
-__device__ __forceinline__ uint64_t mnmajor_step(uint64_t d0, int ks) {
-  return d0 + static_cast<uint64_t>((ks * 2048) >> 4);
-}
-
-// TMEM row (D fp32 columns at taddr) * mul -> 16-bit row `row` of a 128-row
-// tile in shared memory, in the layout a 128-byte-swizzled TMA box expects:
-// 64-column atoms of 128 x 128 bytes, 16-byte chunk c of row r at chunk
-// position c ^ (r mod 8).  Eight consecutive rows cover all 32 banks, so a
-// warp's 16-byte stores are conflict-free.
-template <int D, bool BF16>
-__device__ __forceinline__ void stage_row_from_tmem(uint32_t taddr, uint8_t* tile, int row,
-                                                    float mul) {
-#pragma unroll
-  for (int c = 0; c < D; c += 64) {  // one 64-column atom per TMEM round trip
-    uint32_t v[64];
-    tmem_ld32(taddr + c, v);
-    tmem_ld32(taddr + c + 32, v + 32);
-    tmem_ld_wait();
-    reg_fence<64>(v);
-    uint8_t* rowp = tile + (c / 64) * kAtomBytes + row * 128;
-#pragma unroll
-    for (int ch = 0; ch < 8; ++ch) {  // 16-byte chunk ch: columns c + 8*ch .. +7
-      uint32_t pk[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        pk[e] = pack2<BF16>(__uint_as_float(v[8 * ch + 2 * e]) * mul,
-                            __uint_as_float(v[8 * ch + 2 * e + 1]) * mul);
-      *reinterpret_cast<uint4*>(rowp + ((ch ^ (row & 7)) * 16)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-    }
-  }
-}
-
-// First key tile a causal sliding window of `window` keys exposes to query
-// tile t: its first row, t*128, sees keys t*128 - window + 1 .. t*128.
-__device__ __forceinline__ int window_first_tile(int t, int window) {
-  const int first_key = t * kBlk - window + 1;
-  return first_key > 0 ? first_key / kBlk : 0;
-}
+constexpr int kThreads = 192;  // dQ kernel: 4 compute warps, producer, MMA issuer
 
 // ------------------------------------------------------------------ dK, dV
-template <int D>
-struct DkdvSmem {
-  static constexpr int kTile = kBlk * D * 2;
-  static constexpr int kK = 0;
-  static constexpr int kV = kK + kTile;
-  static constexpr int kQ = kV + kTile;        // 2 stages
-  static constexpr int kdO = kQ + 2 * kTile;   // 2 stages
-  static constexpr int kLse = kdO + 2 * kTile; // 2 stages x 128 floats: -LSE * log2(e)
-  static constexpr int kDrow = kLse + 1024;    // 2 stages x 128 floats: -D
-  static constexpr int kBar = kDrow + 1024;
-  static constexpr int kBytes = kBar + 256;
-  static constexpr int kAlloc = kBytes + 1024;
-};
-
-enum DkdvBars {
-  KB_KV = 0,
-  KB_QFULL = 1,   // +stage: Q_i, dO_i (TMA) and LSE_i, D_i (32 producer lanes)
-  KB_QEMPTY = 3,  // +stage
-  KB_SFULL = 5,   // S^T in TMEM
-  KB_DPFULL = 6,  // dP^T in TMEM
-  KB_PREADY = 7,  // P^T written to TMEM (4 warps)
-  KB_DSREADY = 8, // dS^T written to TMEM (4 warps)
-  KB_DVDONE = 9,  // dV MMA done: S^T columns free
-  KB_DKDONE = 10, // dK MMA done: dP^T columns free
-  KB_FINAL = 11,
-  KB_N = 12
-};
-
-// WIN: causal sliding window of `window` keys (key k visible to query q iff
-// q - window < k <= q): key tile j meets only the query tiles its keys are
-// visible to, and the window's edge is masked element-wise.
+// The key-tile pass (dkdv_body.cuh) without the one-pass dQ share.
 template <int D, bool BF16, bool WIN>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kDkdvThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                        const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
                        const float* __restrict__ lse, const float* __restrict__ Drow, int heads,
                        int head_group, int Hq, int Hkv, int N, int causal, int window, float scale,
                        int* err) {
-  using L = DkdvSmem<D>;
-  constexpr int kAtoms = D / 64;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = align1024(smem_raw);
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::kBar);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + KB_N);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int T = (N + kBlk - 1) / kBlk;
-  // Groups of KV heads whose Q and dO stay in L2; within a group the key tiles
-  // with the most work under causal masking (small j) first.
-  const WorkItem wi = grouped_heavy_first(blockIdx.x, heads, T, head_group);
-  const int j = wi.rank;
-  const int bkv = wi.head;  // b * Hkv + hkv
-  const int b = bkv / Hkv;
-  const int hkv = bkv % Hkv;
-  const int group = Hq / Hkv;
-  const int i0 = causal ? j : 0;
-  // Last query tile that sees a key of tile j: keys up to j*128 + 127 are
-  // visible to queries up to j*128 + 126 + window.
-  int i_last = T - 1;
-  if (WIN) {
-    const int qmax = (j * kBlk + kBlk - 2 + window) / kBlk;
-    i_last = qmax < T - 1 ? qmax : T - 1;
-  }
-  const int n_i = i_last - i0 + 1;
-  const int n_it = group * n_i;
-  constexpr uint32_t kColDV = 0, kColDK = 128, kColS = 256, kColDP = 384;
-
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < KB_N; ++i) {
-      uint32_t cnt = 1;
-      if (i == KB_QFULL || i == KB_QFULL + 1) cnt = 33;
-      if (i == KB_PREADY || i == KB_DSREADY) cnt = 4;
-      mbar_init(&bar[i], cnt);
-    }
-    *abort_flag = 0;  // the producer checks the error word once its first loads are issued
-    fence_mbar_init();
-  }
-  if (warp == 5) {
-    tmem_alloc(tmem_slot, 512);
-    tmem_relinquish();
-  }
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-
-  if (warp == 4) {
-    // ------------------------------------------------------------ producer
-    float* s_lse = reinterpret_cast<float*>(smem + L::kLse);
-    float* s_d = reinterpret_cast<float*>(smem + L::kDrow);
-    int issued = 0;
-    if (lane == 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-      tma_prefetch_desc(&tm_do);
-      const uint64_t pol = l2_policy_evict_first();
-      mbar_expect_tx(&bar[KB_KV], 2 * L::kTile);
-      for (int a = 0; a < kAtoms; ++a) {
-        tma_load_3d(smem + L::kK + a * kAtomBytes, &tm_k, &bar[KB_KV], a * 64, j * kBlk, bkv, pol);
-        tma_load_3d(smem + L::kV + a * kAtomBytes, &tm_v, &bar[KB_KV], a * 64, j * kBlk, bkv, pol);
-      }
-    }
-    const uint64_t pol_q = l2_policy_evict_last();
-    for (int it = 0; it < n_it; ++it) {
-      const int hq = hkv * group + it / n_i;
-      const int i = i0 + it % n_i;
-      const int bhq = b * Hq + hq;
-      const int st = it & 1;
-      bool ok = true;
-      if (lane == 0) {
-        ok = mbar_wait(&bar[KB_QEMPTY + st], ((it >> 1) & 1) ^ 1, abort_flag, err);
-        if (ok) {
-          mbar_expect_tx(&bar[KB_QFULL + st], 2 * L::kTile);
-          for (int a = 0; a < kAtoms; ++a) {
-            tma_load_3d(smem + L::kQ + st * L::kTile + a * kAtomBytes, &tm_q, &bar[KB_QFULL + st],
-                        a * 64, i * kBlk, bhq, pol_q);
-            tma_load_3d(smem + L::kdO + st * L::kTile + a * kAtomBytes, &tm_do, &bar[KB_QFULL + st],
-                        a * 64, i * kBlk, bhq, pol_q);
-          }
-          issued = it + 1;
-          // A CTA that starts after another one raised the error word stops at
-          // its next wait; reading the word only now keeps its latency off the
-          // path to the first MMA.
-          if (it == 0 && *reinterpret_cast<volatile int*>(err) != kDevErrNone) *abort_flag = 1;
-        }
-      }
-      if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) == 0) break;  // also orders the stage reuse
-      // -LSE (as log2) and -D of the tile's 128 query rows, negated so the
-      // compute warps add them; padding rows get LSE = +inf so their recomputed
-      // probabilities are exactly 0.
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int r = lane * 4 + e;
-        const int qrow = i * kBlk + r;
-        const size_t g = static_cast<size_t>(bhq) * N + qrow;
-        const bool in = qrow < N;
-        s_lse[st * 128 + r] = in ? -lse[g] * kLog2e : -INFINITY;
-        s_d[st * 128 + r] = in ? -Drow[g] : 0.f;
-      }
-      mbar_arrive(&bar[KB_QFULL + st]);
-    }
-    if (lane == 0 && *abort_flag) {
-      drain_wait(&bar[KB_KV], 0);
-      for (int it = (issued > 2 ? issued - 2 : 0); it < issued; ++it)
-        drain_wait(&bar[KB_QFULL + (it & 1)], (it >> 1) & 1);
-    }
-  } else if (warp == 5) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t kIdS = idesc_f16(kBlk, kBlk, BF16, false, false);  // S^T, dP^T
-      constexpr uint32_t kIdKV = idesc_f16(kBlk, D, BF16, false, true);     // dV, dK
-      constexpr uint64_t kStageStep = L::kTile >> 4;  // one stage further, in descriptor units
-      const uint64_t dk0 = kmajor_desc(smem_u32(smem + L::kK), 0);
-      const uint64_t dv0 = kmajor_desc(smem_u32(smem + L::kV), 0);
-      const uint64_t dq0 = kmajor_desc(smem_u32(smem + L::kQ), 0);
-      const uint64_t ddo0 = kmajor_desc(smem_u32(smem + L::kdO), 0);
-      const uint64_t mq0 = mnmajor_desc(smem_u32(smem + L::kQ), 0);
-      const uint64_t mdo0 = mnmajor_desc(smem_u32(smem + L::kdO), 0);
-      auto issue_s = [&](int st) {  // S^T = K_j Q_i^T
-        const uint64_t qd = dq0 + st * kStageStep;
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks)
-          mma_ss(tmem + kColS, kmajor_step(dk0, ks), kmajor_step(qd, ks), kIdS, ks > 0);
-        mma_commit(&bar[KB_SFULL]);
-      };
-      auto issue_dp = [&](int st) {  // dP^T = V_j dO_i^T
-        const uint64_t dd = ddo0 + st * kStageStep;
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks)
-          mma_ss(tmem + kColDP, kmajor_step(dv0, ks), kmajor_step(dd, ks), kIdS, ks > 0);
-        mma_commit(&bar[KB_DPFULL]);
-      };
-      bool ok = mbar_wait(&bar[KB_KV], 0, abort_flag, err) &&
-                mbar_wait(&bar[KB_QFULL], 0, abort_flag, err);
-      if (ok) {
-        tc_fence_after();
-        issue_s(0);
-        issue_dp(0);
-      }
-      // Issue order per iteration: dV(it), S^T(it+1), dK(it), dP^T(it+1).  S^T(it+1)
-      // needs only dV(it) finished (it overwrites the P^T columns), so the next
-      // P^T phase can start while this iteration's dS^T is still being computed.
-      for (int it = 0; ok && it < n_it; ++it) {
-        const int st = it & 1;
-        const uint64_t qm = mq0 + st * kStageStep;
-        const uint64_t dom = mdo0 + st * kStageStep;
-        const bool more = it + 1 < n_it;
-        const int st1 = (it + 1) & 1;
-        // dV += P^T dO_i   (P^T: 16-bit pairs over the first half of the S^T columns)
-        if (!(ok = mbar_wait(&bar[KB_PREADY], it & 1, abort_flag, err))) break;
-        tc_fence_after();
-#pragma unroll
-        for (int ks = 0; ks < kBlk / 16; ++ks)
-          mma_ts(tmem + kColDV, tmem + kColS + ks * 8, mnmajor_step(dom, ks), kIdKV,
-                 (it > 0 || ks > 0) ? 1u : 0u);
-        mma_commit(&bar[KB_DVDONE]);
-        if (more) {
-          if (!(ok = mbar_wait(&bar[KB_QFULL + st1], ((it + 1) >> 1) & 1, abort_flag, err))) break;
-          if (!(ok = mbar_wait(&bar[KB_DVDONE], it & 1, abort_flag, err))) break;
-          tc_fence_after();
-          issue_s(st1);
-        }
-        // dK += dS^T Q_i   (dS^T: 16-bit pairs over the first half of the dP^T columns)
-        if (!(ok = mbar_wait(&bar[KB_DSREADY], it & 1, abort_flag, err))) break;
-        tc_fence_after();
-#pragma unroll
-        for (int ks = 0; ks < kBlk / 16; ++ks)
-          mma_ts(tmem + kColDK, tmem + kColDP + ks * 8, mnmajor_step(qm, ks), kIdKV,
-                 (it > 0 || ks > 0) ? 1u : 0u);
-        mma_commit(&bar[KB_DKDONE]);
-        mma_commit(&bar[KB_QEMPTY + st]);
-        if (more) {
-          // dP^T(it+1) overwrites the dS^T columns dK(it) reads.
-          if (!(ok = mbar_wait(&bar[KB_DKDONE], it & 1, abort_flag, err))) break;
-          tc_fence_after();
-          issue_dp(st1);
-        }
-      }
-      mma_commit(&bar[KB_FINAL]);
-      drain_wait(&bar[KB_FINAL], 0);
-    }
-  } else if (warp < 4) {
-    // ------------------------------------------------------------ compute: P^T, dS^T
-    const int t = threadIdx.x;  // key row within the tile
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-    const uint32_t tS = tmem + lane_off + kColS;
-    const uint32_t tP = tmem + lane_off + kColDP;
-    const float sl2 = scale * kLog2e;
-    const uint64_t sl2x2 = f2_pack(sl2, sl2);
-    const float* s_lse = reinterpret_cast<const float*>(smem + L::kLse);
-    const float* s_d = reinterpret_cast<const float*>(smem + L::kDrow);
-    bool ok = true;
-    for (int it = 0; it < n_it; ++it) {
-      const int i = i0 + it % n_i;
-      const int st = it & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(&bar[KB_SFULL], it & 1, abort_flag, err) &&
-                                       mbar_wait(&bar[KB_QFULL + st], (it >> 1) & 1, abort_flag, err));
-      if (!ok) break;
-      tc_fence_after();
-      const bool diag = causal && (i == j);
-      const float* lse2 = s_lse + st * 128;
-      const float* dd = s_d + st * 128;
-      // P^T row t: exp2(s * scale*log2(e) - LSE_q*log2(e)); query q before key t is masked.
-      float p[kBlk];
-#pragma unroll
-      for (int h = 0; h < kBlk; h += 64) {  // two halves keep the live registers below the cap
-        uint32_t sv[64];
-        tmem_ld32(tS + h, sv);
-        tmem_ld32(tS + h + 32, sv + 32);
-        tmem_ld_wait();
-        reg_fence<64>(sv);
-#pragma unroll
-        for (int c = 0; c < 64; c += 4) {
-          const float4 l4 = lds128_ordered(lse2 + h + c);  // -LSE_q * log2(e)
-          float a0, a1, a2, a3;
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sl2x2,
-                           f2_pack(l4.x, l4.y)),
-                    a0, a1);
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3])), sl2x2,
-                           f2_pack(l4.z, l4.w)),
-                    a2, a3);
-          p[h + c] = ex2_approx(a0);
-          p[h + c + 1] = ex2_approx(a1);
-          p[h + c + 2] = ex2_approx(a2);
-          p[h + c + 3] = ex2_approx(a3);
-        }
-      }
-      if (diag) {
-#pragma unroll
-        for (int c = 0; c < kBlk; ++c)
-          if (c < t) p[c] = 0.f;
-      }
-      if (WIN && (i - j) * kBlk + kBlk - 1 >= window) {
-        // The window's edge crosses this tile: query i*128 + c sees key
-        // j*128 + t iff i*128 + c - window < j*128 + t.
-        const int lim_c = (j - i) * kBlk + t + window;
-#pragma unroll
-        for (int c = 0; c < kBlk; ++c)
-          if (c >= lim_c) p[c] = 0.f;
-      }
-#pragma unroll
-      for (int c = 0; c < kBlk; c += 32) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) pk[e] = pack2<BF16>(p[c + 2 * e], p[c + 2 * e + 1]);
-        tmem_st16(tS + c / 2, pk);
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar[KB_PREADY]);
-      // dS^T = P^T o (dP^T - D_q), chunk by chunk; chunk c's 16-bit pairs land
-      // on dP^T columns already read.
-      ok = __all_sync(0xffffffffu, mbar_wait(&bar[KB_DPFULL], it & 1, abort_flag, err));
-      if (!ok) break;
-      tc_fence_after();
-#pragma unroll
-      for (int c = 0; c < kBlk; c += 32) {
-        uint32_t dpv[32];
-        tmem_ld32(tP + c, dpv);
-        tmem_ld_wait();
-        reg_fence<32>(dpv);
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          const float4 d4 = lds128_ordered(dd + c + e);  // -D_q
-          float g0, g1, g2, g3;
-          f2_unpack(f2_mul(f2_pack(p[c + e], p[c + e + 1]),
-                           f2_add(f2_pack(__uint_as_float(dpv[e]), __uint_as_float(dpv[e + 1])),
-                                  f2_pack(d4.x, d4.y))),
-                    g0, g1);
-          f2_unpack(f2_mul(f2_pack(p[c + e + 2], p[c + e + 3]),
-                           f2_add(f2_pack(__uint_as_float(dpv[e + 2]), __uint_as_float(dpv[e + 3])),
-                                  f2_pack(d4.z, d4.w))),
-                    g2, g3);
-          pk[e / 2] = pack2<BF16>(g0, g1);
-          pk[e / 2 + 1] = pack2<BF16>(g2, g3);
-        }
-        tmem_st16(tP + c / 2, pk);
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar[KB_DSREADY]);
-    }
-    // Epilogue: dV and dK leave as 16-bit tiles staged in shared memory and
-    // written by TMA stores.  dV is final once the last dV MMA has completed;
-    // by then every MMA that reads K or V has completed too (they were issued
-    // before it), so dV is staged over K while the last dK MMA still runs,
-    // and dK over V once every MMA is done.
-    const bool store_rows = j * kBlk + 32 * warp < N;  // a store box must start inside the tensor
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bar[KB_DVDONE], (n_it - 1) & 1, abort_flag, err));
-    if (ok) {
-      tc_fence_after();
-      uint8_t* st_dv = smem + L::kK;
-      stage_row_from_tmem<D, BF16>(tmem + lane_off + kColDV, st_dv, t, 1.0f);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0 && store_rows) {
-#pragma unroll
-        for (int a = 0; a < kAtoms; ++a)
-          tma_store_3d(&tm_dv, st_dv + a * kAtomBytes + warp * 4096, a * 64, j * kBlk + 32 * warp, bkv);
-        bulk_commit_group();
-      }
-    }
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bar[KB_FINAL], 0, abort_flag, err));
-    if (ok) {
-      tc_fence_after();
-      uint8_t* st_dk = smem + L::kV;
-      stage_row_from_tmem<D, BF16>(tmem + lane_off + kColDK, st_dk, t, scale);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0 && store_rows) {
-#pragma unroll
-        for (int a = 0; a < kAtoms; ++a)
-          tma_store_3d(&tm_dk, st_dk + a * kAtomBytes + warp * 4096, a * 64, j * kBlk + 32 * warp, bkv);
-        bulk_commit_group();
-      }
-    }
-    // Shared memory stays allocated until every store issued here has read it.
-    if (lane == 0) bulk_wait_read_all();
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 5) {
-    __syncwarp();
-    tc_fence_after();
-    tmem_dealloc(tmem, 512);
-  }
+  dkdv_body<D, BF16, WIN, false>(&tm_q, &tm_k, &tm_v, &tm_do, &tm_dk, &tm_dv, lse, Drow, nullptr, heads,
+                                 head_group, Hq, Hkv, N, causal, window, scale, err);
 }
 
 // ------------------------------------------------------------------ dQ
@@ -886,19 +433,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Heads scheduled side by side so that the operands they stream (per_head_bytes
-// each) stay within about a quarter of the 129 MB L2: 16 heads at N = 4096,
-// d = 128 (2 MB each), 4 at N = 16384.
-int l2_head_group(long per_head_bytes) {
-  long g = (32L << 20) / (per_head_bytes > 0 ? per_head_bytes : 1);
-  return static_cast<int>(g < 1 ? 1 : (g > 64 ? 64 : g));
-}
-
 template <int D, bool BF16, bool WIN>
 cudaError_t launch_bwd_t(const AttnShape& s, const BwdArgs& a, cudaStream_t stream) {
   const int T = (s.N + kBlk - 1) / kBlk;
   auto kdkdv = fa_bwd_dkdv_kernel<D, BF16, WIN>;
-  constexpr int smem_kv = DkdvSmem<D>::kAlloc;
+  constexpr int smem_kv = DkdvSmem<D, false>::kAlloc;
   const int slot = (WIN ? 4 : 0) + (D == 64 ? 0 : 2) + (BF16 ? 1 : 0);
   cudaError_t e;
   if ((e = set_smem_once(reinterpret_cast<const void*>(kdkdv), smem_kv, 8 + slot)) != cudaSuccess)
@@ -916,7 +455,7 @@ cudaError_t launch_bwd_t(const AttnShape& s, const BwdArgs& a, cudaStream_t stre
       s.B * s.Hq, l2_head_group(4L * s.N * D), s.Hq, s.Hkv, s.N, s.causal, s.window, s.scale, a.err);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (a.ev_before_dkdv && (e = cudaEventRecord(a.ev_before_dkdv, stream)) != cudaSuccess) return e;
-  kdkdv<<<dim3(static_cast<unsigned>(T * s.B * s.Hkv)), kThreads, smem_kv, stream>>>(
+  kdkdv<<<dim3(static_cast<unsigned>(T * s.B * s.Hkv)), kDkdvThreads, smem_kv, stream>>>(
       a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dk, a.tm_dv, a.lse, a.D, s.B * s.Hkv,
       l2_head_group(4L * s.N * D * (s.Hq / s.Hkv)), s.Hq, s.Hkv, s.N, s.causal, s.window, s.scale,
       a.err);
@@ -928,7 +467,7 @@ cudaError_t launch_bwd_t(const AttnShape& s, const BwdArgs& a, cudaStream_t stre
 }  // namespace
 
 size_t backward_smem_bytes(int d) {
-  return d == 64 ? DkdvSmem<64>::kAlloc : DkdvSmem<128>::kAlloc;
+  return d == 64 ? DkdvSmem<64, false>::kAlloc : DkdvSmem<128, false>::kAlloc;
 }
 
 cudaError_t launch_backward(const AttnShape& s, const BwdArgs& a, cudaStream_t stream) {

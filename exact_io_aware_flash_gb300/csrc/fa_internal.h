@@ -86,6 +86,11 @@ cudaError_t launch_forward(const AttnShape& s, const FwdArgs& a, cudaStream_t st
 // codes [B*Hkv][d][Np]), d = 128, bfloat16 O.
 cudaError_t launch_forward_fp8(const AttnShape& s, const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_backward(const AttnShape& s, const BwdArgs& a, cudaStream_t stream);
+// One-pass backward (fa_bwd_atomic.cu): a.D and dq_acc ([B*Hq][N][d] fp32) are
+// workspace, overwritten; tm_dq and ev_* as for launch_backward (the events
+// bracket the preprocessing kernel and the main kernel).
+cudaError_t launch_backward_atomic(const AttnShape& s, const BwdArgs& a, float* dq_acc,
+                                   cudaStream_t stream);
 cudaError_t launch_decode(const AttnShape& s, const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_quantize_fp8(const AttnShape& s, const Fp8QuantArgs& a, cudaStream_t stream);
 
@@ -102,6 +107,7 @@ int set_last_error(int code, const char* fmt, ...);
 // Shared-memory bytes the forward kernel needs for head dimension d (for checks).
 size_t forward_smem_bytes(int d);
 size_t backward_smem_bytes(int d);
+size_t backward_atomic_smem_bytes(int d);
 size_t decode_smem_bytes(int d);
 
 }  // namespace fa

@@ -242,6 +242,20 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
       : "r"(taddr));
 }
 
+// Whole-warp load of 16 lanes x 256 bits, four times along the columns: for
+// repeat r, thread t gets lane base + t/4, columns 8r + 2(t mod 4) and +1 in
+// r[4r], r[4r+1], and lane base + 8 + t/4, the same columns, in r[4r+2],
+// r[4r+3].  base must be the first or the middle lane of the warp's 32.
+__device__ __forceinline__ void tmem_ld16x256_x4(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+
 __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* r) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
                "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
@@ -402,6 +416,13 @@ __device__ __forceinline__ WorkItem grouped_heavy_first(int linear, int heads, i
   w.rank = r / gh;
   w.head = g * group + (r - w.rank * gh);
   return w;
+}
+
+// ---------------------------------------------------------------- global reductions
+// Adds (a, b) to the two consecutive floats at p (8-byte aligned) in L2, with
+// no return value; concurrent adds from other threads and CTAs are atomic.
+__device__ __forceinline__ void red_add_f32x2(float* p, float a, float b) {
+  asm volatile("red.global.add.v2.f32 [%0], {%1, %2};" ::"l"(p), "f"(a), "f"(b) : "memory");
 }
 
 // ---------------------------------------------------------------- math

@@ -27,6 +27,8 @@ def main():
     ap.add_argument("--fp16", action="store_true")
     ap.add_argument("--noncausal", action="store_true")
     ap.add_argument("--forward-only", action="store_true")
+    ap.add_argument("--atomic", action="store_true",
+                    help="backward through fa_backward_atomic (one pass, dQ by atomic adds)")
     ap.add_argument("--fp8", action="store_true", help="e4m3 quantization + forward instead")
     ap.add_argument("--decode", type=int, default=0, metavar="NK",
                     help="split-KV decoding instead: one query row per head against NK keys")
@@ -62,7 +64,7 @@ def main():
     for _ in range(a.iters):
         o, lse = forward(q, k, v, causal=causal, scale=scale)
         if not a.forward_only:
-            backward(q, k, v, o, lse, dO, causal=causal, scale=scale)
+            backward(q, k, v, o, lse, dO, causal=causal, scale=scale, deterministic=not a.atomic)
     torch.cuda.synchronize()
     check_errors()
     print(f"profile_case done: {shape} causal={causal} iters={a.iters}")

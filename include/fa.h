@@ -213,6 +213,48 @@ FA_API int fa_backward_window(const void* q, const void* k, const void* v, const
                               int d, int window, float scale, int dtype, void* stream);
 
 /*
+ * Bytes of device workspace fa_backward_atomic needs: round_up(4 * B*Hq*N, 256)
+ * + round_up(4 * B*Hq*N*d, 256).  Returns 0 if the sizes are invalid.  Layout:
+ * D float32 [B, Hq, N] at offset 0, then the float32 dQ accumulator
+ * [B, Hq, N, d].
+ */
+FA_API size_t fa_backward_atomic_workspace_size(int B, int Hq, int N, int d);
+
+/*
+ * Backward pass in one sweep over the key tiles, with dQ accumulated across
+ * thread blocks by atomic adds: the primer's default backward ("FlashAttention
+ * Primer: IO-Aware Attention, from FA1 to FA4", section "Backward pass:
+ * recomputation instead of storage", which notes that it is bitwise
+ * nondeterministic and that the deterministic form is slower).
+ *
+ * Same inputs and outputs as fa_backward; `causal` as there and `window` as in
+ * fa_backward_window (0: none; >= 1 needs causal = 1; window >= N is causal).
+ * Steps, all on `stream`:
+ *   1. D_i = rowsum(dO_i * O_i) into the workspace, and the workspace's dQ
+ *      accumulator set to zero;
+ *   2. per key/value tile j: recompute S^T, P^T and dS^T against every query
+ *      tile i that sees it (and every query head of the KV head), accumulate
+ *      dV += P^T dO and dK += scale * dS^T Q in one CTA, and add the partial
+ *      dQ_i += dS K_j into the accumulator with float32 atomic adds;
+ *   3. dq = scale * accumulator, rounded to dtype.
+ * Five N x N x d products per tile pair instead of fa_backward's seven.  dk
+ * and dv are summed in a fixed order (bitwise reproducible); dq is the same
+ * sum in an order that varies between runs, so its last bits may differ from
+ * run to run and from fa_backward's.
+ *
+ * workspace: at least fa_backward_atomic_workspace_size() bytes of device
+ * memory, 256-byte aligned, owned by the caller, not used concurrently by
+ * another call.  Errors as fa_backward, plus FA_ERR_INVALID for window < 0 or
+ * window > 0 with causal = 0.  The event hooks of
+ * fa_set_backward_event_hooks bracket step 1 (before_dq .. before_dkdv) and
+ * step 2 (before_dkdv .. after_dkdv).
+ */
+FA_API int fa_backward_atomic(const void* q, const void* k, const void* v, const void* o,
+                              const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                              void* workspace, size_t ws_bytes, int B, int Hq, int Hkv, int N,
+                              int d, int causal, int window, float scale, int dtype, void* stream);
+
+/*
  * Backward pass that allocates nothing.  (Library-side addition: the attention
  * method has no counterpart of it.)
  *
