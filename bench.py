@@ -557,7 +557,9 @@ FWD_TARGET, BWD_TARGET = 0.60, 0.45
 
 def workload_table(dev, peaks):
     """Device time and throughput of every evaluation workload: the four forward
-    workloads (with % of HBM for the two short-N ones) and the backward sweep."""
+    workloads (with % of HBM for the two short-N ones) and the backward sweep
+    (deterministic two-pass backward; at N = 4096 and 16384 also the one-pass
+    atomic backward)."""
     import torch
 
     from exact_io_aware_flash_gb300 import backward, forward, forward_splitkv, workspace_size
@@ -618,6 +620,16 @@ def workload_table(dev, peaks):
              "tflops": fl / ms / 1e9, "pct_of_bf16_burst": fl / ms / 1e9 / burst}
         if N >= 4096:
             e.update({"target_pct": BWD_TARGET, "target_met": fl / ms / 1e9 / burst >= BWD_TARGET})
+        if N in (4096, 16384):
+            # the one-pass backward (dQ summed with atomic adds) on the same inputs
+            ws_a = torch.empty(workspace_size(s.B, s.Hq, s.N, s.d, deterministic=False),
+                               dtype=torch.uint8, device=dev)
+            ms_a = _graph_time(lambda: backward(q, k, v, o, lse, dO, causal=True, dq=dq, dk=dk,
+                                                dv=dv, workspace=ws_a, deterministic=False),
+                               iters=10)
+            e["atomic_one_pass"] = {"ms": ms_a, "tflops": fl / ms_a / 1e9,
+                                    "pct_of_bf16_burst": fl / ms_a / 1e9 / burst}
+            del ws_a
         bwd[f"N{N}"] = e
         del q, k, v, dO, o, lse, ws, dq, dk, dv
     out["backward_sweep"] = bwd
