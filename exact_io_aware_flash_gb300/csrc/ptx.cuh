@@ -425,6 +425,13 @@ __device__ __forceinline__ void red_add_f32x2(float* p, float a, float b) {
   asm volatile("red.global.add.v2.f32 [%0], {%1, %2};" ::"l"(p), "f"(a), "f"(b) : "memory");
 }
 
+// One 32-byte store (a whole L2 sector) from one thread; p must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t* w) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]), "r"(w[1]),
+               "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
 // ---------------------------------------------------------------- math
 // Packed two-wide fp32 arithmetic (one instruction for two lanes of work on
 // sm_100-class GPUs).  A pair lives in one 64-bit register: low = first.
