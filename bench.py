@@ -146,8 +146,8 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ traffic
-KERNEL_SOURCES = {"fa_bwd_dkdv_kernel": ("fa_bwd.cu", "ptx.cuh"),
-                  "fa_bwd_dq_kernel": ("fa_bwd.cu", "ptx.cuh"),
+KERNEL_SOURCES = {"fa_bwd_dkdv_kernel": ("fa_bwd.cu", "dkdv_body.cuh", "bwd_common.cuh", "ptx.cuh"),
+                  "fa_bwd_dq_kernel": ("fa_bwd.cu", "dkdv_body.cuh", "bwd_common.cuh", "ptx.cuh"),
                   "fa_fwd_kernel": ("fa_fwd.cu", "ptx.cuh")}
 
 
