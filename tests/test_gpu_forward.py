@@ -148,6 +148,28 @@ def test_forward_is_deterministic_and_writes_every_output():
     assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
 
 
+@pytest.mark.parametrize("B,Hq,Hkv,N,d,causal", [(1, 2, 1, 300, 64, True), (2, 2, 2, 257, 128, False),
+                                                  (1, 4, 4, 1000, 128, True)])
+def test_forward_output_16_byte_aligned_only(B, Hq, Hkv, N, d, causal):
+    """O whose base is 16- but not 32-byte aligned (the ABI's minimum) takes the
+    kernel's 16-byte store path: same bits as a 32-byte aligned O, and the oracle."""
+    shape = Shape(B, Hq, Hkv, N, d)
+    inp = make_inputs(shape, "bf16", seed=11 + N, with_dO=False)
+    q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
+    scale = 1.0 / math.sqrt(d)
+    o_al, lse_al = forward(q, k, v, causal=causal, scale=scale)
+    n = B * Hq * N * d
+    base = torch.full((n + 16,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    o_16 = base[8:8 + n].view(B, Hq, N, d)  # 16-byte offset from a 256-byte aligned allocation
+    assert o_16.data_ptr() % 16 == 0 and o_16.data_ptr() % 32 != 0 and o_al.data_ptr() % 32 == 0
+    _, lse_16 = forward(q, k, v, causal=causal, scale=scale, out=o_16)
+    check_errors()
+    assert torch.equal(o_16, o_al) and torch.equal(lse_16, lse_al)
+    assert torch.isnan(base[:8].float()).all() and torch.isnan(base[8 + n:].float()).all()
+    o_ref, lse_ref = oracle.forward(inp["q"], inp["k"], inp["v"], causal, scale)
+    assert_matches(o_16, lse_16, o_ref, lse_ref, "bf16", f"{shape} causal={causal}, 16-byte aligned O")
+
+
 def test_forward_rejects_bad_arguments():
     q = torch.zeros(1, 2, 64, 96, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(FAError) as e:
