@@ -18,6 +18,7 @@
 // saturation) is an exactly rounded IEEE operation, so the codes are a definite
 // function of the inputs.
 #include "fa_internal.h"
+#include "ptx.cuh"
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -39,6 +40,11 @@ __device__ __forceinline__ float to_f32(uint16_t bits) {
 
 __device__ __forceinline__ uint32_t e4m3(float x) {
   return static_cast<uint32_t>(__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3));
+}
+
+// Two codes, lo in the low byte (round to nearest even, saturated, like e4m3()).
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3));
 }
 
 // Q and K, d = 128.  One CTA (8 warps) per (tensor, head, 128-row block).  A
@@ -76,48 +82,74 @@ __global__ void __launch_bounds__(kQkThreads)
       raw[g][c] = r < N ? *reinterpret_cast<const uint4*>(src + static_cast<size_t>(r) * D + 32 * sub + 8 * c)
                         : make_uint4(0u, 0u, 0u, 0u);
   }
-  float y[2][32];
+  // A lane's 32 channels as 16 packed pairs (channels 2k, 2k+1).  The packed
+  // fp32 operations round each half exactly as the scalar ones would, so the
+  // codes are the same as a scalar butterfly's; the kernel is issue-bound and
+  // the pairs halve most of its instructions.
+  const uint64_t one2 = f2_pack(1.0f, 1.0f);
+  const uint64_t neg1x2 = f2_pack(-1.0f, -1.0f);
+  uint64_t sgn2[16];  // the random signs of this lane's channels, as packed +-1
+  if (signs) {
+#pragma unroll
+    for (int k = 0; k < 16; ++k)
+      sgn2[k] = f2_pack(signs[32 * sub + 2 * k] < 0 ? -1.0f : 1.0f, signs[32 * sub + 2 * k + 1] < 0 ? -1.0f : 1.0f);
+  }
+  uint64_t y[2][16];
   float amax = 0.f;
 #pragma unroll
   for (int g = 0; g < 2; ++g) {
-    float* a = y[g];
+    uint64_t* A = y[g];
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       const uint32_t w[4] = {raw[g][c].x, raw[g][c].y, raw[g][c].z, raw[g][c].w};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        a[8 * c + 2 * e] = to_f32<BF16>(static_cast<uint16_t>(w[e] & 0xFFFFu));
-        a[8 * c + 2 * e + 1] = to_f32<BF16>(static_cast<uint16_t>(w[e] >> 16));
-      }
+      for (int e = 0; e < 4; ++e)
+        A[4 * c + e] = f2_pack(to_f32<BF16>(static_cast<uint16_t>(w[e] & 0xFFFFu)),
+                               to_f32<BF16>(static_cast<uint16_t>(w[e] >> 16)));
     }
     if (signs) {
 #pragma unroll
-      for (int e = 0; e < 32; ++e)
-        if (signs[32 * sub + e] < 0) a[e] = -a[e];
+      for (int k = 0; k < 16; ++k) A[k] = f2_mul(A[k], sgn2[k]);  // exact: x * (+-1)
       // Butterfly stage h pairs channel i (bit h clear) with i + h: (a + b, a - b).
+      // h = 1 inside each pair:
 #pragma unroll
-      for (int h = 1; h < 32; h <<= 1) {
+      for (int k = 0; k < 16; ++k) {
+        float lo, hi;
+        f2_unpack(A[k], lo, hi);
+        A[k] = f2_pack(lo + hi, lo - hi);
+      }
+      // h = 2 .. 16: pair k with pair k + h/2; a - b as fma(b, -1, a), one rounding.
 #pragma unroll
-        for (int e = 0; e < 32; ++e)
-          if ((e & h) == 0) {
-            const float lo = a[e], hi = a[e + h];
-            a[e] = lo + hi;
-            a[e + h] = lo - hi;
+      for (int hp = 1; hp < 16; hp <<= 1) {
+#pragma unroll
+        for (int k = 0; k < 16; ++k)
+          if ((k & hp) == 0) {
+            const uint64_t lo = A[k], hi = A[k + hp];
+            A[k] = f2_add(lo, hi);
+            A[k + hp] = f2_fma(hi, neg1x2, lo);
           }
       }
-      // h = 32, 64: channel 32s + e pairs with 32(s ^ m) + e, m = h / 32.
+      // h = 32, 64: channel 32s + e pairs with 32(s ^ m) + e, m = h / 32: the
+      // lower lane keeps a + other, the upper one other - a, both as
+      // fma(a, +-1, other).
 #pragma unroll
       for (int m = 1; m < 4; m <<= 1) {
-        const bool lower = (sub & m) == 0;
+        const uint64_t sg = (sub & m) == 0 ? one2 : neg1x2;
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const float other = __shfl_xor_sync(0xffffffffu, a[e], m);
-          a[e] = lower ? a[e] + other : other - a[e];
+        for (int k = 0; k < 16; ++k) {
+          float lo, hi;
+          f2_unpack(A[k], lo, hi);
+          const uint64_t other = f2_pack(__shfl_xor_sync(0xffffffffu, lo, m), __shfl_xor_sync(0xffffffffu, hi, m));
+          A[k] = f2_fma(A[k], sg, other);
         }
       }
     }
 #pragma unroll
-    for (int e = 0; e < 32; ++e) amax = fmaxf(amax, fabsf(a[e]));
+    for (int k = 0; k < 16; ++k) {
+      float lo, hi;
+      f2_unpack(A[k], lo, hi);
+      amax = fmax3(amax, fabsf(lo), fabsf(hi));
+    }
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
@@ -127,6 +159,7 @@ __global__ void __launch_bounds__(kQkThreads)
 #pragma unroll
   for (int w = 1; w < kQkThreads / 32; ++w) amax = fmaxf(amax, s_max[w]);
   const float f = amax > 0.f ? 448.0f / amax : 0.f;
+  const uint64_t f2 = f2_pack(f, f);
   if (threadIdx.x == 0) (is_q ? q_scale : k_scale)[blk] = amax * cfac;
 #pragma unroll
   for (int g = 0; g < 2; ++g) {
@@ -134,9 +167,12 @@ __global__ void __launch_bounds__(kQkThreads)
     if (r < N) {
       uint32_t c[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e)
-        c[e] = e4m3(y[g][4 * e] * f) | (e4m3(y[g][4 * e + 1] * f) << 8) |
-               (e4m3(y[g][4 * e + 2] * f) << 16) | (e4m3(y[g][4 * e + 3] * f) << 24);
+      for (int e = 0; e < 8; ++e) {  // channels 4e .. 4e+3, the lowest in the lowest byte
+        float v0, v1, v2, v3;
+        f2_unpack(f2_mul(y[g][2 * e], f2), v0, v1);
+        f2_unpack(f2_mul(y[g][2 * e + 1], f2), v2, v3);
+        c[e] = e4m3x2(v0, v1) | (e4m3x2(v2, v3) << 16);
+      }
       uint4* o = reinterpret_cast<uint4*>(dst + static_cast<size_t>(r) * D + 32 * sub);
       o[0] = make_uint4(c[0], c[1], c[2], c[3]);
       o[1] = make_uint4(c[4], c[5], c[6], c[7]);
