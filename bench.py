@@ -30,6 +30,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import shutil
 import subprocess
@@ -146,16 +147,32 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ traffic
-KERNEL_SOURCES = {"fa_bwd_dkdv_kernel": ("fa_bwd.cu", "dkdv_body.cuh", "bwd_common.cuh", "ptx.cuh"),
-                  "fa_bwd_dq_kernel": ("fa_bwd.cu", "dkdv_body.cuh", "bwd_common.cuh", "ptx.cuh"),
-                  "fa_fwd_kernel": ("fa_fwd.cu", "ptx.cuh")}
+KERNEL_FILES = {"fa_bwd_dkdv_kernel": "fa_bwd.cu", "fa_bwd_dq_kernel": "fa_bwd.cu",
+                "fa_fwd_kernel": "fa_fwd.cu"}
+CSRC = os.path.join(ROOT, "exact_io_aware_flash_gb300", "csrc")
+
+
+def kernel_sources(kernel: str) -> list:
+    """The .cu file that defines `kernel`, then every header of the package it
+    includes directly or through other headers (sorted)."""
+    top = KERNEL_FILES[kernel]
+    seen, todo = set(), [top]
+    while todo:
+        with open(os.path.join(CSRC, todo.pop()), encoding="utf-8") as f:
+            text = f.read()
+        for inc in re.findall(r'#include\s+"([^"]+)"', text):
+            name = os.path.basename(inc)
+            if name not in seen and os.path.exists(os.path.join(CSRC, name)):
+                seen.add(name)
+                todo.append(name)
+    return [top] + sorted(seen - {top})
 
 
 def kernel_sources_digest(kernel: str) -> str:
     """Digest of the source files that define `kernel`."""
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(ROOT, "exact_io_aware_flash_gb300", "csrc", name), "rb") as f:
+    for name in kernel_sources(kernel):
+        with open(os.path.join(CSRC, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
