@@ -115,3 +115,34 @@ def test_planted_mistake_is_caught(tmp_path, name, old, new):
 def test_unmutated_oracle_passes_the_same_checks(tmp_path):
     lib = oracle.build(force=True, src=SRC, out=str(tmp_path / "lib_clean.so"))
     assert not _checks_fail(oracle.Oracle(lib))
+
+
+def _key_shift_invariance_fails(o: "oracle.Oracle") -> bool:
+    """The key-shift pin alone: shifting every key by one vector must leave dQ
+    unchanged (rows of dS sum to zero), for causal, non-causal and windowed
+    attention."""
+    rng = np.random.default_rng(7)
+    B, Hq, Hkv, N, d, s = 1, 2, 1, 7, 4, 0.9
+    q, k, v, dO = (rng.standard_normal(x) for x in
+                   ((B, Hq, N, d), (B, Hkv, N, d), (B, Hkv, N, d), (B, Hq, N, d)))
+    c = rng.standard_normal((B, Hkv, 1, d))
+    for causal in (False, True):
+        dq, _, _, _ = o.backward(q, k, v, dO, causal, s)
+        dq2, _, _, _ = o.backward(q, k + c, v, dO, causal, s)
+        if not np.allclose(dq, dq2, atol=1e-10):
+            return True
+    dq, _, _ = o.backward_window(q, k, v, dO, 3, s)
+    dq2, _, _ = o.backward_window(q, k + c, v, dO, 3, s)
+    return not np.allclose(dq, dq2, atol=1e-10)
+
+
+@pytest.mark.parametrize("name", ["drop_D_term", "window_backward_drops_D"])
+def test_key_shift_pin_catches_a_dropped_D(tmp_path, name):
+    old, new = next((m[1], m[2]) for m in MUTATIONS if m[0] == name)
+    text = open(SRC).read()
+    src = tmp_path / f"oracle_{name}.c"
+    src.write_text(text.replace(old, new))
+    lib = oracle.build(force=True, src=str(src), out=str(tmp_path / f"lib_{name}.so"))
+    assert _key_shift_invariance_fails(oracle.Oracle(lib))
+    clean = oracle.build(force=True, src=SRC, out=str(tmp_path / "lib_clean.so"))
+    assert not _key_shift_invariance_fails(oracle.Oracle(clean))

@@ -163,6 +163,28 @@ def test_noncausal_key_permutation_invariance():
 
 
 @pytest.mark.parametrize("causal", [False, True])
+def test_key_shift_invariance(causal):
+    """Adding one vector c to every key of a KV head adds scale * q_i . c to all
+    of row i's scores: P and O are unchanged and LSE_i moves by scale * q_i . c.
+    dS is unchanged, so dK and dV are too, and dQ_i = scale * sum_k dS_ik k_k is
+    unchanged only because every row of dS sums to zero (the softmax-Jacobian
+    term -D_i makes it so)."""
+    B, Hq, Hkv, N, d, s = 2, 4, 2, 11, 6, 0.7
+    q, k, v, dO = rand(B, Hq, N, d), rand(B, Hkv, N, d), rand(B, Hkv, N, d), rand(B, Hq, N, d)
+    c = rand(B, Hkv, 1, d)
+    o, lse = oracle.forward(q, k, v, causal, s)
+    o2, lse2 = oracle.forward(q, k + c, v, causal, s)
+    g = Hq // Hkv
+    shift = s * np.einsum("bhnd,bhd->bhn", q, np.repeat(c[:, :, 0, :], g, axis=1))
+    np.testing.assert_allclose(o2, o, atol=1e-12)
+    np.testing.assert_allclose(lse2, lse + shift, atol=1e-12)
+    dq, dk, dv, _ = oracle.backward(q, k, v, dO, causal, s)
+    dq2, dk2, dv2, _ = oracle.backward(q, k + c, v, dO, causal, s)
+    for a, b in ((dq2, dq), (dk2, dk), (dv2, dv)):
+        np.testing.assert_allclose(a, b, atol=1e-11)
+
+
+@pytest.mark.parametrize("causal", [False, True])
 def test_gradient_invariants(causal):
     B, Hq, Hkv, N, d = 1, 4, 2, 9, 5
     q, k, v, dO = rand(B, Hq, N, d), rand(B, Hkv, N, d), rand(B, Hkv, N, d), rand(B, Hq, N, d)
